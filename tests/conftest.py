@@ -1,0 +1,23 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a CUDA GPU (sm_103a) and the built libhg.so")
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The C-ABI library, built in-tree; GPU tests only."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fp8_mxfp4_grouped_gb300 import hg
+    return hg
