@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark of the grouped FP8 x MXFP4 MoE GEMM hot path (routing plan + GEMM).
+
+Workload (default): the gate/up projection of the pages' headline table --
+E=32 experts, top-8, N=4096, K=6144, unbalanced (biased) routing -- swept over
+M in {64, 256, 512, 768, 1152, 1536, 2048} tokens.  One step = for every M:
+routing plan + grouped GEMM, each launch pair preceded by an L2 flush (a
+write of 2x the L2 size), timed with CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  value = total GEMM FLOPs of the sweep /
+device time of plan+GEMM launches (TFLOP/s, whole job).  The reference arm
+(--impl reference) times the CPU oracle on a bounded sample of the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "grouped FP8×MXFP4 MoE GEMM µs & TFLOP/s vs tokens M; % of roofline"
+UNIT = "TFLOP/s"
+CONFIG_ID = 1
+WORKLOAD = "gate_up E=32 top8 N=4096 K=6144 unbalanced, M sweep 64..2048"
+FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor ratio
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sust=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
+
+
+def algorithmic(R, E_act, E, N, K):
+    """GEMM flops and the bytes each operand must cross HBM once."""
+    flops = 2.0 * R * N * K
+    byts = (E_act * N * K / 2 + E_act * N * K / 32 + R * K + R * K / 128 + 2.0 * R * N
+            + 4.0 * (E + 1))
+    return flops, byts
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def reduce_scalar(x: float, op: str, world: int) -> float:
+    """Max or sum of a per-rank scalar over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background during timing."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm --
+
+def run_ours(args, rank, world):
+    from fp8_mxfp4_grouped_gb300 import hg
+    from oracle.plan import plan_expert_offsets  # bookkeeping only (E_act), not timed
+    from synth import make_case
+    from synth.inputs import CONFIGS
+
+    dev = torch.device("cuda")
+    cfg = CONFIGS[CONFIG_ID]
+    Ms = args.Ms or cfg["Ms"]
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16"] * FP8_OVER_BF16
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+
+    cases = []
+    for M in Ms:
+        c = make_case(CONFIG_ID, M, device=dev)
+        off, *_ = plan_expert_offsets(c.topk_ids, c.E)
+        e_act = int(np.count_nonzero(np.diff(off)))
+        R = c.R
+        ids = torch.from_numpy(c.topk_ids).to(dev)
+        bufs = dict(
+            ids=ids,
+            off=torch.empty(c.E + 1, dtype=torch.int32, device=dev),
+            s2d=torch.empty(R, dtype=torch.int32, device=dev),
+            d2s=torch.empty(R, dtype=torch.int32, device=dev),
+            ws=torch.empty(max(4, hg.hg_plan_workspace_bytes(M, c.top_k, c.E)),
+                           dtype=torch.uint8, device=dev),
+            out=torch.empty((R, c.N), dtype=torch.bfloat16, device=dev),
+        )
+        # pinned host copies for the end-to-end leg
+        host = dict(ids=torch.from_numpy(c.topk_ids).pin_memory(),
+                    a=c.a_fp8.cpu().pin_memory(), a_s=c.a_scale.cpu().pin_memory(),
+                    out=torch.empty((R, c.N), dtype=torch.bfloat16).pin_memory())
+        flops, byts = algorithmic(R, e_act, c.E, c.N, c.K)
+        cases.append(dict(M=M, c=c, R=R, e_act=e_act, flops=flops, bytes=byts, bufs=bufs,
+                          host=host))
+
+    def launch(cs, s):
+        b = cs["bufs"]
+        c = cs["c"]
+        hg.hg_plan_expert_offsets(b["ids"], c.E, b["off"], b["s2d"], b["d2s"], b["ws"], stream=s)
+        hg.hg_grouped_w4a8_gemm(c.a_fp8, c.a_scale, c.w_fp4, c.w_scale, b["off"], out=b["out"],
+                                stream=s)
+
+    def one_step(record):
+        times = []
+        for cs in cases:
+            with torch.cuda.stream(stream):
+                flush.fill_(cs["M"] & 0xFF)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e2 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                c = cs["c"]
+                b = cs["bufs"]
+                hg.hg_plan_expert_offsets(b["ids"], c.E, b["off"], b["s2d"], b["d2s"], b["ws"],
+                                          stream=stream)
+                e1.record(stream)
+                hg.hg_grouped_w4a8_gemm(c.a_fp8, c.a_scale, c.w_fp4, c.w_scale, b["off"],
+                                        out=b["out"], stream=stream)
+                e2.record(stream)
+            times.append((e0, e1, e2))
+        if record is not None:
+            record.append(times)
+
+    for _ in range(args.warmup):
+        one_step(None)
+    torch.cuda.synchronize()
+    st, detail = hg.hg_get_device_status()
+    if st != hg.HG_OK:
+        raise RuntimeError(f"device status {st} detail {detail} after warm-up")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    recs = []
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step(recs)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+
+    plan_us = [[] for _ in cases]
+    gemm_us = [[] for _ in cases]
+    for times in recs:
+        for i, (e0, e1, e2) in enumerate(times):
+            plan_us[i].append(e0.elapsed_time(e1) * 1e3)
+            gemm_us[i].append(e1.elapsed_time(e2) * 1e3)
+    st, detail = hg.hg_get_device_status()
+    if st != hg.HG_OK:
+        raise RuntimeError(f"device status {st} detail {detail} after timing")
+
+    device_s = sum(sum(p) + sum(g) for p, g in zip(plan_us, gemm_us)) * 1e-6   # all K steps
+    flops_step = sum(cs["flops"] for cs in cases)
+    dev_max = reduce_scalar(device_s, "max", world)
+    flops_all = reduce_scalar(flops_step * args.steps, "sum", world)
+    value = flops_all / dev_max / 1e12
+
+    sweep = []
+    for i, cs in enumerate(cases):
+        g = statistics.median(gemm_us[i])
+        p = statistics.median(plan_us[i])
+        t_hbm = cs["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_tc = cs["flops"] / (fp8_peak * 1e12)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        sweep.append(dict(M=cs["M"], R=cs["R"], E_act=cs["e_act"], gemm_us=round(g, 2),
+                          plan_us=round(p, 2), tflops=round(cs["flops"] / g / 1e6, 1),
+                          gbs=round(cs["bytes"] / g / 1e3, 1), bound=bound,
+                          roof_frac=round(max(t_hbm, t_tc) / (g * 1e-6), 3)))
+    dom = max(range(len(cases)), key=lambda i: statistics.median(gemm_us[i]))
+    dcs = cases[dom]
+    dg = statistics.median(gemm_us[dom]) * 1e-6
+    if sweep[dom]["bound"] == "tensor":
+        roof = dict(bound="tensor", achieved=round(dcs["flops"] / dg / 1e12, 1),
+                    peak=round(fp8_peak, 1), unit="TFLOP/s")
+    else:
+        roof = dict(bound="hbm", achieved=round(dcs["bytes"] / dg / 1e9, 1),
+                    peak=peaks["hbm_gbs"], unit="GB/s")
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
+    roof["traffic"] = args.traffic
+    roof["launch"] = f"GEMM at M={dcs['M']} (largest share of the step)"
+    roof["peak_source"] = (f"{peaks['source']}: bf16 {peaks['bf16']} TFLOP/s x{FP8_OVER_BF16} "
+                           f"nominal fp8/bf16" if roof["bound"] == "tensor"
+                           else f"{peaks['source']} HBM copy")
+    roof["sweep_roof_time_frac"] = round(
+        sum(max(cs["bytes"] / (peaks["hbm_gbs"] * 1e9), cs["flops"] / (fp8_peak * 1e12))
+            for cs in cases) / (sum(statistics.median(g) for g in gemm_us) * 1e-6), 3)
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        def e2e_step():
+            evs = []
+            for cs in cases:
+                b, h, c = cs["bufs"], cs["host"], cs["c"]
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    b["ids"].copy_(h["ids"], non_blocking=True)
+                    c.a_fp8.copy_(h["a"], non_blocking=True)
+                    c.a_scale.copy_(h["a_s"], non_blocking=True)
+                    launch(cs, stream)
+                    h["out"].copy_(b["out"], non_blocking=True)
+                    e1.record(stream)
+                evs.append((e0, e1))
+            return evs
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(args.steps):
+            evs = e2e_step()
+            torch.cuda.synchronize()
+            tot += sum(a.elapsed_time(b) for a, b in evs) * 1e-3
+        tot = reduce_scalar(tot, "max", world)
+        bi = sum(cs["c"].topk_ids.nbytes + cs["c"].a_fp8.numel() + cs["c"].a_scale.numel()
+                 for cs in cases)
+        bo = sum(cs["bufs"]["out"].numel() * 2 for cs in cases)
+        e2e = dict(value=round(flops_all / tot / 1e12, 2), unit=UNIT, h2d_bytes_per_step=int(bi),
+                   d2h_bytes_per_step=int(bo))
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(Ms[0])
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dev_max / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 x fp4e2m1 -> f32 acc -> bf16",
+        "data": "synthetic (seeded routing, N(0,1) values quantised as the configs state)",
+        "config": {"workload": WORKLOAD, "E": 32, "top_k": 8, "N": 4096, "K": 6144,
+                   "Ms": Ms, "routing": "biased (unbalanced)",
+                   "l2": "flushed before every plan+GEMM pair (write of 2x L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "sweep": sweep,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * len(cases) * args.steps,
+        "clocks": clk,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    return line
+
+
+# ------------------------------------------------------------ oracle arms --
+
+def cpu_baseline(M, budget_s=30.0):
+    """The CPU oracle as it stands on a bounded sample: plan + full GEMM of M tokens."""
+    from oracle import gemm as G
+    from oracle.plan import plan_expert_offsets
+    from synth import make_case
+    c = make_case(CONFIG_ID, M, device="cpu", cache_weights=False)
+    a, a_s = c.a_fp8.numpy(), c.a_scale.numpy()
+    w, w_s = c.w_fp4.numpy(), c.w_scale.numpy()
+    t0 = time.perf_counter()
+    off, *_ = plan_expert_offsets(c.topk_ids, c.E)
+    G.grouped_w4a8_gemm(a, a_s, w, w_s, off, c.E, c.N, c.K)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * c.R * c.N * c.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"gate/up M={M} (R={c.R}): plan + full float64 GEMM over all experts, "
+                      f"{dt:.1f} s; numpy decode single-threaded, matmul on the host BLAS "
+                      f"threads ({os.cpu_count()} cores)"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    from oracle import gemm as G
+    from oracle.plan import plan_expert_offsets
+    from synth import make_case
+    M = 64
+    c = make_case(CONFIG_ID, M, device="cpu", cache_weights=False)
+    a, a_s = c.a_fp8.numpy(), c.a_scale.numpy()
+    w, w_s = c.w_fp4.numpy(), c.w_scale.numpy()
+    # bounded sample per step: the experts of the first 2 tokens' routing
+    off, *_ = plan_expert_offsets(c.topk_ids, c.E)
+    sel = sorted(set(int(x) for x in c.topk_ids[:2].ravel()))
+    flops_step = sum(2.0 * (off[e + 1] - off[e]) * c.N * c.K for e in sel)
+
+    def step():
+        o, *_ = plan_expert_offsets(c.topk_ids, c.E)
+        for e in sel:
+            lo, hi = int(o[e]), int(o[e + 1])
+            sub = np.array([0, hi - lo], dtype=np.int64)
+            G.grouped_w4a8_gemm(a[lo:hi], a_s[lo:hi], w[e:e + 1], w_s[e:e + 1], sub, 1, c.N, c.K)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    v = flops_step * args.steps / dt / 1e12
+    sample = (f"gate/up M={M}: plan + float64 GEMM of the {len(sel)} experts routed by the first "
+              f"2 tokens ({int(sum(off[e + 1] - off[e] for e in sel))} rows) per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "kind": "oracle",
+                         "cores": os.cpu_count(), "sample": sample},
+        "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--Ms", type=lambda s: [int(x) for x in s.split(",")], default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the dominant GEMM launch, if measured")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, world, _ = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,264 @@
+// api.cu -- the extern "C" entry points of libhg (declared in include/hg.h):
+// argument validation (before any CUDA call), the plan launch configuration
+// (shared-memory fit), TMA tensor-map encoding, and the device status word.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "hg_internal.cuh"
+
+namespace hg {
+namespace {
+
+// Library-owned status word; one instance per device (module-scope device
+// variable), addressed through cudaGetSymbolAddress.
+__device__ uint32_t g_status[kStatusWords];
+
+constexpr int kMaxDevices = 64;
+constexpr int kPlanMaxThreads = 512;
+constexpr int kPlanIdsPerBlock = 2048;
+constexpr int kPlanMaxBlocks = 256;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int smem_optin = 0;
+    uint32_t* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+
+hg_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HG_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return HG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return HG_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+            return HG_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return HG_ERR_CUDA;
+        d.status = static_cast<uint32_t*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return HG_OK;
+}
+
+hg_status encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        }
+    });
+    if (!g_encode) return HG_ERR_CUDA;
+    *fn = g_encode;
+    return HG_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int plan_nblk(long long R) {
+    long long n = (R + kPlanIdsPerBlock - 1) / kPlanIdsPerBlock;
+    if (n < 1) n = 1;
+    if (n > kPlanMaxBlocks) n = kPlanMaxBlocks;
+    return static_cast<int>(n);
+}
+
+}  // namespace
+}  // namespace hg
+
+using namespace hg;
+
+extern "C" {
+
+const char* hg_status_string(int status) {
+    switch (status) {
+        case HG_OK: return "ok";
+        case HG_ERR_INVALID_ARG: return "invalid argument";
+        case HG_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case HG_ERR_RESOURCE: return "resource limit exceeded";
+        case HG_ERR_CUDA: return "CUDA error";
+        case HG_ERR_TIMEOUT: return "device wait timed out";
+        case HG_ERR_BAD_OFFSETS: return "expert offsets not monotone or beyond rows";
+        case HG_ERR_BAD_IDS: return "expert id out of range";
+        default: return "unknown status";
+    }
+}
+
+int hg_version(void) { return 100; }
+
+size_t hg_plan_workspace_bytes(int32_t M, int32_t top_k, int32_t E) {
+    if (M < 0 || top_k < 1 || E < 1) return 0;
+    const long long R = static_cast<long long>(M) * top_k;
+    if (R > 0x7FFFFFFFll) return 0;
+    return static_cast<size_t>(plan_nblk(R)) * static_cast<size_t>(E) * sizeof(int32_t);
+}
+
+int32_t hg_plan_block_threads(int32_t E, int32_t smem_limit_bytes) {
+    if (E < 1 || smem_limit_bytes <= 0) return 0;
+    for (int t = kPlanMaxThreads; t >= 32; t -= 32) {
+        if (plan_smem_bytes(E, t) <= static_cast<size_t>(smem_limit_bytes)) return t;
+    }
+    return 0;
+}
+
+hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t E,
+                                 int32_t* expert_offsets, int32_t* sorted_to_src,
+                                 int32_t* src_to_sorted, void* workspace, size_t workspace_bytes,
+                                 hg_stream_t stream) {
+    if (M < 0 || top_k < 1 || E < 1) return HG_ERR_INVALID_ARG;
+    const long long R = static_cast<long long>(M) * top_k;
+    if (R > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_offsets) return HG_ERR_INVALID_ARG;
+    if (R > 0 && (!topk_ids || !sorted_to_src || !src_to_sorted)) return HG_ERR_INVALID_ARG;
+    const size_t need = hg_plan_workspace_bytes(M, top_k, E);
+    if (R > 0 && (!workspace || workspace_bytes < need)) return HG_ERR_INVALID_ARG;
+    if (R > 0 && !aligned(workspace, 4)) return HG_ERR_INVALID_ARG;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (R == 0) {
+        return cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s) == cudaSuccess
+                   ? HG_OK
+                   : HG_ERR_CUDA;
+    }
+    DeviceInfo* d = nullptr;
+    hg_status st = device_info(&d);
+    if (st != HG_OK) return st;
+    const int threads = hg_plan_block_threads(E, d->smem_optin);
+    if (threads == 0) return HG_ERR_RESOURCE;
+    const int nblk = plan_nblk(R);
+    const int step = threads;   // chunk is a multiple of 32 ids per warp
+    long long chunk = (R + nblk - 1) / nblk;
+    chunk = ((chunk + step - 1) / step) * step;
+    PlanArgs a;
+    a.ids = topk_ids;
+    a.R = static_cast<int32_t>(R);
+    a.E = E;
+    a.offsets = expert_offsets;
+    a.sorted_to_src = sorted_to_src;
+    a.src_to_sorted = src_to_sorted;
+    a.ws_counts = static_cast<int32_t*>(workspace);
+    a.status = d->status;
+    a.threads = threads;
+    a.nblk = nblk;
+    a.chunk = static_cast<int>(chunk);
+    return launch_plan(a, s) == cudaSuccess ? HG_OK : HG_ERR_CUDA;
+}
+
+hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
+                               const uint8_t* w_fp4, const uint8_t* w_scale,
+                               const int32_t* expert_offsets, int32_t E, int32_t N, int32_t K,
+                               int32_t rows, uint16_t* out_bf16, hg_stream_t stream) {
+    if (E < 1 || N < 1 || K < 1 || rows < 0) return HG_ERR_INVALID_ARG;
+    if (!w_fp4 || !w_scale || !expert_offsets) return HG_ERR_INVALID_ARG;
+    if (rows > 0 && (!a_fp8 || !a_scale || !out_bf16)) return HG_ERR_INVALID_ARG;
+    if (E > gemm_max_experts() || N % 128 != 0 || K % 512 != 0) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<long long>(E) * N > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(w_fp4, 32) || !aligned(w_scale, 4)) return HG_ERR_INVALID_ARG;
+    if (rows > 0 && (!aligned(a_fp8, 16) || !aligned(out_bf16, 2))) return HG_ERR_INVALID_ARG;
+    if (rows == 0) return HG_OK;
+
+    DeviceInfo* d = nullptr;
+    hg_status st = device_info(&d);
+    if (st != HG_OK) return st;
+    if (static_cast<int>(gemm_smem_bytes(E)) > d->smem_optin) return HG_ERR_RESOURCE;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    st = encoder(&encode);
+    if (st != HG_OK) return st;
+
+    // Weights: [E*N rows, K elements] of E2M1, unpacked by the TMA into one
+    // 16-byte chunk (8 data bytes + 8 pad) per 16 elements, 128-byte swizzle.
+    CUtensorMap map_w, map_a;
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K),
+                              static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+        cuuint32_t box[2] = {128, 128};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(w_fp4),
+                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return HG_ERR_CUDA;
+    }
+    // Activations: [rows, K] bytes, 16-row x 128-byte boxes, 128-byte swizzle.
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+        cuuint32_t box[2] = {128, 16};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a_fp8), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return HG_ERR_CUDA;
+    }
+    GemmArgs a;
+    a.a_fp8 = a_fp8;
+    a.a_scale = a_scale;
+    a.w_fp4 = w_fp4;
+    a.w_scale = w_scale;
+    a.offsets = expert_offsets;
+    a.E = E;
+    a.N = N;
+    a.K = K;
+    a.rows = rows;
+    a.out = out_bf16;
+    a.status = d->status;
+    a.timeout_ns = g_timeout_ns.load();
+    a.num_sms = d->num_sms;
+    return launch_grouped_gemm(a, map_w, map_a, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? HG_OK
+               : HG_ERR_CUDA;
+}
+
+hg_status hg_get_device_status(hg_stream_t stream, uint32_t* detail) {
+    DeviceInfo* d = nullptr;
+    hg_status st = device_info(&d);
+    if (st != HG_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return HG_ERR_CUDA;
+    uint32_t host[kStatusWords] = {0, 0, 0, 0};
+    if (cudaMemcpy(host, d->status, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return HG_ERR_CUDA;
+    const uint32_t zero[kStatusWords] = {0, 0, 0, 0};
+    if (cudaMemcpy(d->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return HG_ERR_CUDA;
+    if (detail) *detail = host[kStatusCode] == HG_ERR_BAD_IDS ? host[kStatusBadIds] : host[kStatusDetail];
+    return static_cast<hg_status>(host[kStatusCode]);
+}
+
+hg_status hg_selftest_wait_timeout(uint32_t timeout_us, hg_stream_t stream) {
+    DeviceInfo* d = nullptr;
+    hg_status st = device_info(&d);
+    if (st != HG_OK) return st;
+    const uint64_t ns = static_cast<uint64_t>(timeout_us ? timeout_us : 1000u) * 1000ull;
+    return launch_selftest_wait(d->status, ns, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? HG_OK
+               : HG_ERR_CUDA;
+}
+
+void hg_set_wait_timeout_us(uint32_t timeout_us) {
+    g_timeout_ns.store(timeout_us ? static_cast<uint64_t>(timeout_us) * 1000ull : 1000000000ull);
+}
+
+}  // extern "C"

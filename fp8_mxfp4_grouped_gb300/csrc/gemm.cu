@@ -1,0 +1,452 @@
+// gemm.cu -- grouped-contiguous FP8 E4M3 x MXFP4 E2M1 GEMM on tcgen05.
+//
+// What is computed follows humming PR #129 ("perf(sm90): size grouped W4A8
+// tiles per expert"): benchmark command (float8e4m3 activations with one
+// float8e8m0 scale per row per 128-K group, float4e2m1 weights with one
+// float8e8m0 scale per output column per 32-K group, bfloat16 output,
+// grouped_contiguous rows) and its first section (the tile is sized from the
+// rows of each expert, not from the total row count).
+//
+// Design (GB300 / sm_103a):
+//  * swap-AB: the weight rows of one expert (128 per tile) are the MMA's M
+//    side, the expert's routed tokens are the MMA's N side.  N can be any
+//    multiple of 16 up to 256, so each expert's token tile is sized from its
+//    own row count at instruction granularity: an expert with 130 rows gets
+//    one 144-token tile, not two 128-row tiles.
+//  * one persistent CTA per SM walks a unit list (expert, weight-row tile,
+//    token tile) built on the device from expert_offsets; no host sync.
+//  * warp roles: warp 0 issues TMA loads (weights through the 16U4_ALIGN16B
+//    unpacking TMA type, activations as bytes; no multicast); warps 2,3,8,9
+//    stage the block scales into the tensor core's scale layout (activation
+//    scales are per 128-K, replicated into the four 32-K blocks they cover);
+//    warp 1 copies scales to TMEM and issues tcgen05.mma kind::mxf8f6f4 with
+//    block scaling, accumulating FP32 in TMEM; warps 4..7 drain the TMEM
+//    accumulator (double-buffered) to BF16 with stores cut at the expert's
+//    last row.
+//  * every barrier wait is bounded (see wait_bounded).
+#include <cuda_bf16.h>
+
+#include "hg_internal.cuh"
+
+namespace hg {
+namespace {
+
+constexpr int kBK = 128;              // K per pipeline stage = one activation-scale group
+constexpr int kBW = 128;              // weight rows per tile (MMA M)
+constexpr int kTMax = 224;            // largest token tile (MMA N), multiple of 16
+constexpr int kStages = 4;
+constexpr int kSfWarps = 4;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 320;         // 10 warps
+constexpr int kABoxRows = 16;         // rows per activation TMA box
+constexpr int kMaxE = 1024;
+
+constexpr uint32_t kWTileBytes = kBW * kBK;    // unpacked E2M1: one byte of smem per element
+// The 16U4_ALIGN16B TMA load writes 8 data bytes into each 16-byte chunk and
+// leaves the other 8 untouched; its transaction count is the packed bytes.
+constexpr uint32_t kWTileTx = kBW * kBK / 2;
+constexpr uint32_t kATileBytes = kTMax * kBK;
+constexpr uint32_t kABoxBytes = kABoxRows * kBK;
+constexpr uint32_t kSfaBytes = 512;            // 128 rows x 4 blocks of 32 K
+constexpr uint32_t kSfbBytes = 1024;           // up to 256 tokens x 4 blocks
+constexpr uint32_t kAccCols = kTMax;           // TMEM columns per accumulator buffer
+constexpr uint32_t kSfCol0 = 2 * kAccCols;     // scale factors after both accumulators
+constexpr uint32_t kSfSlotCols = 12;           // 4 (weights) + 8 (tokens) per stage
+constexpr uint32_t kTmemCols = 512;
+static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "TMEM budget");
+static_assert(kSfWarps == kStages, "one scale warp per ring slot");
+
+constexpr uint32_t kOffW = 0;
+constexpr uint32_t kOffA = kOffW + kStages * kWTileBytes;
+constexpr uint32_t kOffSfa = kOffA + kStages * kATileBytes;
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
+constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
+constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kOffSched = kOffMisc + 64;
+static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
+
+struct Sched {
+    const int32_t* start;
+    const int32_t* rows;
+    const int32_t* ntt;
+    const int32_t* tile;
+    const int32_t* prefix;   // [E+1] exclusive prefix of units per expert
+    int E;
+    int NT;                  // weight-row tiles per expert (N / 128)
+};
+
+struct Unit {
+    int e;
+    int n0;      // first weight row (output column)
+    int row0;    // first sorted row of the token tile
+    int nrows;   // valid rows of the tile
+    int n_mma;   // MMA N: nrows rounded up to 16
+};
+
+__device__ __forceinline__ Unit decode_unit(const Sched& s, int u) {
+    int lo = 0, hi = s.E;   // prefix[lo] <= u < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s.prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    Unit t;
+    t.e = lo;
+    const int local = u - s.prefix[lo];
+    const int ntt = s.ntt[lo];
+    const int nt = local / ntt;
+    const int tt = local - nt * ntt;
+    const int tile = s.tile[lo];
+    t.n0 = nt * kBW;
+    t.row0 = s.start[lo] + tt * tile;
+    t.nrows = min(tile, s.rows[lo] - tt * tile);
+    t.n_mma = (t.nrows + 15) & ~15;
+    return t;
+}
+
+__device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) {
+    return __ldg(reinterpret_cast<const uint32_t*>(p));
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Bounded wait that ignores the abort flag: used while draining in-flight
+// asynchronous work before the CTA exits.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
+                    const __grid_constant__ CUtensorMap map_a,
+                    const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
+                    const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
+                    uint16_t* __restrict__ out, uint32_t* status, uint64_t timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (sbase - raw_u32);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t bar_full_tma = sbase + kOffBar;
+    const uint32_t bar_full_sf = bar_full_tma + 8 * kStages;
+    const uint32_t bar_empty = bar_full_sf + 8 * kStages;
+    const uint32_t bar_tfull = bar_empty + 8 * kStages;
+    const uint32_t bar_tempty = bar_tfull + 16;
+    const uint32_t bar_done = bar_tempty + 16;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
+    int32_t* s_start = reinterpret_cast<int32_t*>(base + kOffSched);
+    int32_t* s_rows = s_start + E;
+    int32_t* s_ntt = s_rows + E;
+    int32_t* s_tile = s_ntt + E;
+    int32_t* s_prefix = s_tile + E;   // E + 1 entries
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar_full_tma + 8 * s, 1);
+            ptx::mbar_init(bar_full_sf + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_tfull + 8 * b, 1);
+            ptx::mbar_init(bar_tempty + 8 * b, kEpiWarps);
+        }
+        ptx::mbar_init(bar_done, 1);
+        misc[1] = 0u;   // abort flag
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(sbase + kOffMisc, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&map_w);
+        ptx::prefetch_tensormap(&map_a);
+    }
+
+    // Per-expert token tiling, from the expert's own row count.
+    const int NT = N / kBW;
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        const int lo = offsets[e];
+        const int hi = offsets[e + 1];
+        int r = 0;
+        if (lo < 0 || hi < lo || hi > rows) {
+            record_error(status, HG_ERR_BAD_OFFSETS, static_cast<uint32_t>(e));
+        } else {
+            r = hi - lo;
+        }
+        const int ntt = (r + kTMax - 1) / kTMax;
+        const int tile = ntt ? ((((r + ntt - 1) / ntt) + 15) & ~15) : 0;
+        s_start[e] = lo;
+        s_rows[e] = r;
+        s_ntt[e] = ntt;
+        s_tile[e] = tile;
+        s_prefix[e] = ntt * NT;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int c = 0; c < E; c += 32) {
+            const int e = c + lane;
+            const int v = e < E ? s_prefix[e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (e < E) s_prefix[e] = carry + incl - v;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) s_prefix[E] = carry;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    const uint32_t tmem_base = misc[0];
+    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT};
+    const int U = s_prefix[E];
+    const int KT = K / kBK;
+    const WaitCtx wctx{status, misc + 1, timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_a = ptx::policy_evict_last();
+            uint32_t g = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+                const Unit t = decode_unit(sch, u);
+                const int wrow = t.e * N + t.n0;
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const uint32_t slot = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1u;
+                    if (!wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleProducer, slot)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full_tma + 8 * slot;
+                    ptx::mbar_arrive_expect_tx(fb, kWTileTx + t.n_mma * kBK);
+                    ptx::tma_load_2d(sbase + kOffW + slot * kWTileBytes, &map_w, ks * kBK, wrow, fb,
+                                     pol_w);
+                    const uint32_t adst = sbase + kOffA + slot * kATileBytes;
+                    for (int j = 0; j < t.n_mma / kABoxRows; ++j) {
+                        ptx::tma_load_2d(adst + j * kABoxBytes, &map_a, ks * kBK,
+                                         t.row0 + j * kABoxRows, fb, pol_a);
+                    }
+                }
+            }
+            // No copy may land after the CTA exits: wait for the last ring's
+            // worth of issued loads (all of them on the normal path already).
+            const uint32_t first = g > kStages ? g - kStages : 0;
+            for (uint32_t gg = first; gg < g; ++gg) {
+                wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer ---
+        if (lane == 0) {
+            uint32_t g = 0, tc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < U; u += gridDim.x, ++tc) {
+                const Unit t = decode_unit(sch, u);
+                const uint32_t b = tc & 1u;
+                if (!wait_bounded(bar_tempty + 8 * b, ((tc >> 1) & 1u) ^ 1u, wctx, kRoleMma,
+                                  0x100u | b)) {
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t idesc0 =
+                    ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, kBW, t.n_mma);
+                const uint32_t d_tmem = tmem_base + b * kAccCols;
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const uint32_t slot = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1u;
+                    if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
+                        !wait_bounded(bar_full_sf + 8 * slot, ph, wctx, kRoleMma, 0x10u | slot)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sf_col = tmem_base + kSfCol0 + slot * kSfSlotCols;
+                    const uint32_t sfa = sbase + kOffSfa + slot * kSfaBytes;
+                    const uint32_t sfb = sbase + kOffSfb + slot * kSfbBytes;
+                    ptx::tc_cp_32x128b_warpx4(sf_col, ptx::desc_sf_32x16(sfa));
+                    ptx::tc_cp_32x128b_warpx4(sf_col + 4, ptx::desc_sf_32x16(sfb));
+                    if (t.n_mma > 128) {
+                        ptx::tc_cp_32x128b_warpx4(sf_col + 8, ptx::desc_sf_32x16(sfb + 512));
+                    }
+                    const uint32_t wsm = sbase + kOffW + slot * kWTileBytes;
+                    const uint32_t asm_ = sbase + kOffA + slot * kATileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk) {
+                        ptx::mma_mxf8f6f4_1x(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
+                                             ptx::desc_kmajor_sw128(asm_ + kk * 32),
+                                             ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
+                                             sf_col + 4, (ks | kk) != 0 ? 1u : 0u);
+                    }
+                    ptx::tc_commit(bar_empty + 8 * slot);
+                }
+                if (!ok) break;
+                ptx::tc_commit(bar_tfull + 8 * b);
+            }
+            // Everything issued must finish before TMEM is released.
+            ptx::tc_commit(bar_done);
+            wait_drain(bar_done, 0u, timeout_ns);
+        }
+    } else if (warp >= 4 && warp < 4 + kEpiWarps) {
+        // ---------------------------------------------------- epilogue --
+        const int q = warp & 3;   // TMEM lane quadrant this warp may read
+        uint32_t tc = 0;
+        for (int u = blockIdx.x; u < U; u += gridDim.x, ++tc) {
+            const Unit t = decode_unit(sch, u);
+            const uint32_t b = tc & 1u;
+            if (!wait_bounded(bar_tfull + 8 * b, (tc >> 1) & 1u, wctx, kRoleEpilogue, b)) break;
+            ptx::tc_fence_after();
+            const int n = t.n0 + 32 * q + lane;
+            uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kAccCols;
+            for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+                uint32_t v[16];
+                ptx::tmem_ld_32x32b_x16(taddr + c0, v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (c0 + j < t.nrows) {
+                        dst[static_cast<size_t>(c0 + j) * N] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_tempty + 8 * b);
+        }
+    } else {
+        // ------------------------------------------- scale staging -----
+        const int sfw = (warp == 2) ? 0 : (warp == 3) ? 1 : (warp == 8) ? 2 : 3;
+        const int ws_row = K / 32;     // bytes per w_scale row
+        const int as_row = K / kBK;    // bytes per a_scale row
+        uint32_t g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+            const Unit t = decode_unit(sch, u);
+            const uint8_t* wsrc = w_scale + static_cast<size_t>(t.e * N + t.n0 + lane) * ws_row;
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                if (static_cast<int>(g % kSfWarps) != sfw) continue;
+                const uint32_t slot = g % kStages;
+                const uint32_t ph = (g / kStages) & 1u;
+                // Weight scales: row n = lane + 32c, the four 32-K blocks of
+                // this stage in one 32-bit word (byte i = block i).
+                uint32_t wv[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    wv[c] = ldg_u32(wsrc + static_cast<size_t>(32 * c) * ws_row + ks * 4);
+                }
+                // Token scales: one per 128-K group, replicated into the four
+                // 32-K blocks.  Token index = 128a + lane + 32c.
+                uint32_t av[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int tok = 128 * (i >> 2) + lane + 32 * (i & 3);
+                    const int r = t.row0 + tok;
+                    av[i] = 0x7F7F7F7Fu;
+                    if (tok < t.n_mma && r < rows) {
+                        av[i] = static_cast<uint32_t>(
+                                    __ldg(a_scale + static_cast<size_t>(r) * as_row + ks)) *
+                                0x01010101u;
+                    }
+                }
+                if (!wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleScale, slot)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sfa = sbase + kOffSfa + slot * kSfaBytes + 16 * lane;
+                const uint32_t sfb = sbase + kOffSfb + slot * kSfbBytes + 16 * lane;
+                sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
+                sts_v4(sfb, av[0], av[1], av[2], av[3]);
+                if (t.n_mma > 128) sts_v4(sfb + 512, av[4], av[5], av[6], av[7]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_full_sf + 8 * slot);
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    const uint32_t b = ptx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        abort_flag = 0u;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtx ctx{status, &abort_flag, timeout_ns};
+        // Nobody arrives on this barrier: the wait must give up and report.
+        wait_bounded(b, 0u, ctx, kRoleSelftest, 0u);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int32_t E) {
+    return kOffSched + static_cast<size_t>(5 * E + 1) * sizeof(int32_t) + 1024;
+}
+
+int gemm_max_experts() { return kMaxE; }
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
+                                const CUtensorMap& map_a, cudaStream_t stream) {
+    const size_t smem = gemm_smem_bytes(a.E);
+    static int configured_smem = 0;   // the attribute is per function, process-wide
+    if (static_cast<int>(smem) > configured_smem) {
+        cudaError_t err = cudaFuncSetAttribute(grouped_w4a8_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(gemm_smem_bytes(kMaxE)));
+        if (err != cudaSuccess) return err;
+        configured_smem = static_cast<int>(gemm_smem_bytes(kMaxE));
+    }
+    // Upper bound on the number of units: every non-empty expert needs at
+    // most ceil(rows_e / kTMax) token tiles <= rows_e / kTMax + 1.
+    const long long nt = a.N / kBW;
+    const long long active = a.E < a.rows ? a.E : a.rows;
+    const long long units_max = ((a.rows + kTMax - 1) / kTMax + active) * nt;
+    int grid = a.num_sms;
+    if (units_max < grid) grid = static_cast<int>(units_max);
+    if (grid < 1) return cudaSuccess;
+    grouped_w4a8_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_a, a.a_scale, a.w_scale,
+                                                           a.offsets, a.E, a.N, a.K, a.rows, a.out,
+                                                           a.status, a.timeout_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace hg

@@ -1,0 +1,101 @@
+// hg_internal.cuh -- declarations shared by the library's translation units:
+// the device status word protocol, the bounded barrier wait, and the host
+// launchers each kernel file exports to the C-ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hg.h"
+#include "ptx.cuh"
+
+namespace hg {
+
+// Device status word (3 x uint32, library-owned, one per device):
+//   [0] first error code recorded since the last read (0 = none)
+//   [1] detail of that first error
+//   [2] number of expert ids dropped by the plan (out of range)
+enum { kStatusCode = 0, kStatusDetail = 1, kStatusBadIds = 2, kStatusWords = 4 };
+
+__device__ __forceinline__ void record_error(uint32_t* status, uint32_t code, uint32_t detail) {
+    if (atomicCAS(&status[kStatusCode], 0u, code) == 0u) {
+        atomicExch(&status[kStatusDetail], detail);
+    }
+}
+
+// Where a wait happened, packed into the status detail of a timeout:
+// role in bits 24..31, ring slot / buffer in bits 0..23.
+enum WaitRole : uint32_t {
+    kRoleProducer = 1,
+    kRoleScale = 2,
+    kRoleMma = 3,
+    kRoleEpilogue = 4,
+    kRoleTeardown = 5,
+    kRoleSelftest = 6,
+};
+
+struct WaitCtx {
+    uint32_t* status;             // device status word
+    volatile uint32_t* abort;     // shared-memory abort flag of this CTA
+    uint64_t timeout_ns;
+};
+
+// Wait for the phase of `bar` with parity `parity` to complete.  Gives up
+// after ctx.timeout_ns (records HG_ERR_TIMEOUT and raises the CTA's abort
+// flag) or as soon as another role of the CTA raised the abort flag.
+// Returns true when the phase completed.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+                                             uint32_t role, uint32_t where) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*ctx.abort) return false;
+        if ((it & 7u) == 0u && ptx::globaltimer_ns() - t0 > ctx.timeout_ns) {
+            *ctx.abort = 1u;
+            record_error(ctx.status, HG_ERR_TIMEOUT, (role << 24) | (where & 0xFFFFFFu));
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------- host-side launchers --
+
+struct GemmArgs {
+    const uint8_t* a_fp8;
+    const uint8_t* a_scale;
+    const uint8_t* w_fp4;
+    const uint8_t* w_scale;
+    const int32_t* offsets;
+    int32_t E, N, K, rows;
+    uint16_t* out;
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int num_sms;
+};
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
+                                const CUtensorMap& map_a, cudaStream_t stream);
+size_t gemm_smem_bytes(int32_t E);
+int gemm_max_experts();
+
+struct PlanArgs {
+    const int32_t* ids;
+    int32_t R, E;
+    int32_t* offsets;
+    int32_t* sorted_to_src;
+    int32_t* src_to_sorted;
+    int32_t* ws_counts;
+    uint32_t* status;
+    int threads;   // block size chosen by the shared-memory fit
+    int nblk;      // number of blocks of the histogram / scatter grids
+    int chunk;     // ids per block (multiple of 32)
+};
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+size_t plan_smem_bytes(int32_t E, int threads);
+
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace hg

@@ -1,0 +1,144 @@
+"""Python binding of libhg (the C ABI in include/hg.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  Tensors are torch CUDA tensors (device memory and
+streams only); their data pointers are passed straight through ctypes.
+There is no fallback: if the library is missing, importing this module
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhg.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python -m fp8_mxfp4_grouped_gb300.build` (nvcc, sm_103a)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_u32 = ctypes.c_uint32
+_sz = ctypes.c_size_t
+
+lib.hg_status_string.argtypes = [ctypes.c_int]
+lib.hg_status_string.restype = ctypes.c_char_p
+lib.hg_version.argtypes = []
+lib.hg_version.restype = ctypes.c_int
+lib.hg_plan_workspace_bytes.argtypes = [_i32, _i32, _i32]
+lib.hg_plan_workspace_bytes.restype = _sz
+lib.hg_plan_block_threads.argtypes = [_i32, _i32]
+lib.hg_plan_block_threads.restype = _i32
+lib.hg_plan_expert_offsets.argtypes = [_p, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]
+lib.hg_plan_expert_offsets.restype = ctypes.c_int
+lib.hg_grouped_w4a8_gemm.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _p]
+lib.hg_grouped_w4a8_gemm.restype = ctypes.c_int
+lib.hg_get_device_status.argtypes = [_p, ctypes.POINTER(_u32)]
+lib.hg_get_device_status.restype = ctypes.c_int
+lib.hg_selftest_wait_timeout.argtypes = [_u32, _p]
+lib.hg_selftest_wait_timeout.restype = ctypes.c_int
+lib.hg_set_wait_timeout_us.argtypes = [_u32]
+lib.hg_set_wait_timeout_us.restype = None
+
+HG_OK = 0
+HG_ERR_INVALID_ARG = 1
+HG_ERR_UNSUPPORTED_SHAPE = 2
+HG_ERR_RESOURCE = 3
+HG_ERR_CUDA = 4
+HG_ERR_TIMEOUT = 5
+HG_ERR_BAD_OFFSETS = 6
+HG_ERR_BAD_IDS = 7
+
+
+class HgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {lib.hg_status_string(status).decode()} ({status})")
+
+
+def _check(status: int, what: str):
+    if status != HG_OK:
+        raise HgError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def hg_plan_workspace_bytes(M: int, top_k: int, E: int) -> int:
+    return int(lib.hg_plan_workspace_bytes(M, top_k, E))
+
+
+def hg_plan_block_threads(E: int, smem_limit_bytes: int) -> int:
+    return int(lib.hg_plan_block_threads(E, smem_limit_bytes))
+
+
+def hg_plan_expert_offsets(topk_ids: torch.Tensor, E: int, expert_offsets=None,
+                           sorted_to_src=None, src_to_sorted=None, workspace=None,
+                           stream=None):
+    """Routing plan on the GPU. Returns (expert_offsets, sorted_to_src, src_to_sorted)."""
+    assert topk_ids.dtype == torch.int32 and topk_ids.is_contiguous() and topk_ids.dim() == 2
+    M, k = topk_ids.shape
+    dev = topk_ids.device
+    R = M * k
+    if expert_offsets is None:
+        expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if sorted_to_src is None:
+        sorted_to_src = torch.empty(R, dtype=torch.int32, device=dev)
+    if src_to_sorted is None:
+        src_to_sorted = torch.empty(R, dtype=torch.int32, device=dev)
+    need = hg_plan_workspace_bytes(M, k, E)
+    if workspace is None:
+        workspace = torch.empty(max(need, 4), dtype=torch.uint8, device=dev)
+    st = lib.hg_plan_expert_offsets(_ptr(topk_ids), M, k, E, _ptr(expert_offsets),
+                                    _ptr(sorted_to_src), _ptr(src_to_sorted), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "hg_plan_expert_offsets")
+    return expert_offsets, sorted_to_src, src_to_sorted
+
+
+def hg_grouped_w4a8_gemm(a_fp8: torch.Tensor, a_scale: torch.Tensor, w_fp4: torch.Tensor,
+                         w_scale: torch.Tensor, expert_offsets: torch.Tensor, out=None,
+                         stream=None) -> torch.Tensor:
+    """Grouped-contiguous W4A8 GEMM. Returns out [rows, N] as torch.bfloat16."""
+    E, N, K2 = w_fp4.shape
+    K = 2 * K2
+    rows = a_fp8.shape[0]
+    for t in (a_fp8, a_scale, w_fp4, w_scale, expert_offsets):
+        assert t.is_contiguous()
+    assert a_fp8.shape == (rows, K) and a_scale.shape == (rows, K // 128)
+    assert w_scale.shape == (E, N, K // 32) and expert_offsets.numel() == E + 1
+    if out is None:
+        out = torch.empty((rows, N), dtype=torch.bfloat16, device=a_fp8.device)
+    st = lib.hg_grouped_w4a8_gemm(_ptr(a_fp8), _ptr(a_scale), _ptr(w_fp4), _ptr(w_scale),
+                                  _ptr(expert_offsets), E, N, K, rows, _ptr(out),
+                                  _stream(stream))
+    _check(st, "hg_grouped_w4a8_gemm")
+    return out
+
+
+def hg_get_device_status(stream=None):
+    """(status, detail) of the device status word; synchronises the stream."""
+    detail = _u32(0)
+    st = lib.hg_get_device_status(_stream(stream), ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def hg_selftest_wait_timeout(timeout_us: int, stream=None):
+    _check(lib.hg_selftest_wait_timeout(timeout_us, _stream(stream)), "hg_selftest_wait_timeout")
+
+
+def hg_set_wait_timeout_us(timeout_us: int):
+    lib.hg_set_wait_timeout_us(timeout_us)

@@ -1,0 +1,57 @@
+"""Host mirror of the GEMM kernel's per-expert token tiling.
+
+The kernel builds the same table on the device from expert_offsets (see
+``csrc/gemm.cu``); this mirror exists for tests and for the bench's
+bookkeeping (units per launch, padded MMA columns).
+
+Rule (humming PR #129, "perf(sm90): size grouped W4A8 tiles per expert",
+first section: size the M tile from each expert's own rows so unevenly
+routed experts do not pay for mostly empty tiles), restated for the swap-AB
+tcgen05 kernel where an expert's tokens are the MMA's N side:
+
+    n_t(e)  = ceil(rows_e / T_MAX)                    token tiles of expert e
+    tile(e) = round_up_16(ceil(rows_e / n_t(e)))      rows per token tile
+    the last tile of an expert issues MMA N = round_up_16(rows left)
+
+With T_MAX = 224 an expert with 130 rows takes one 144-column tile where a
+fixed 128-row tile would take two.
+"""
+from __future__ import annotations
+
+T_MAX = 224
+MMA_N_STEP = 16
+W_TILE = 128
+
+
+def expert_tiling(rows_e: int):
+    """(n_t, tile) for one expert; (0, 0) for an empty expert."""
+    if rows_e <= 0:
+        return 0, 0
+    n_t = -(-rows_e // T_MAX)
+    per = -(-rows_e // n_t)
+    tile = -(-per // MMA_N_STEP) * MMA_N_STEP
+    return n_t, tile
+
+
+def token_tiles(rows_e: int):
+    """List of (first_row, valid_rows, mma_n) of one expert's token tiles."""
+    n_t, tile = expert_tiling(rows_e)
+    out = []
+    for tt in range(n_t):
+        r0 = tt * tile
+        valid = min(tile, rows_e - r0)
+        out.append((r0, valid, -(-valid // MMA_N_STEP) * MMA_N_STEP))
+    return out
+
+
+def units(offsets, N: int):
+    """Work units of one launch: (expert, n0, first sorted row, valid rows, mma_n)."""
+    E = len(offsets) - 1
+    out = []
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        tiles = token_tiles(hi - lo)
+        for nt in range(N // W_TILE):
+            for (r0, valid, mma_n) in tiles:
+                out.append((e, nt * W_TILE, lo + r0, valid, mma_n))
+    return out

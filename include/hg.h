@@ -1,0 +1,166 @@
+/*
+ * hg.h -- C ABI of libhg: grouped-contiguous FP8 x MXFP4 (W4A8) MoE expert
+ * GEMM and its routing plan, for NVIDIA GB300 (sm_103a).
+ *
+ * Every entry point takes plain pointers and sizes.  All array pointers are
+ * DEVICE pointers owned by the caller unless stated otherwise; the library
+ * never allocates or frees caller memory and never synchronises inside the
+ * compute calls, so they can be enqueued on any stream (including inside a
+ * CUDA-graph capture).  Errors are returned as hg_status codes; nothing is
+ * thrown across this interface.  Argument checks happen before any CUDA call,
+ * so a bad argument is reported even on a machine without a GPU.
+ *
+ * Sources the operations follow (web pages, cited by title and section):
+ *  [H129] humming PR #129 "perf(sm90): size grouped W4A8 tiles per expert" --
+ *         benchmark command (operand formats, group sizes 128 and 32,
+ *         grouped_contiguous layout) and first section (rows of one expert
+ *         are one contiguous range; tile size per expert, not from total
+ *         rows).
+ *  [M38]  MoonEP PR #38 "fit planning block size to device SMEM limit" --
+ *         the planning kernel (per-expert histogram, per-warp scratch of
+ *         (E+1) x (warps+1) counts, per-expert placement), the block size
+ *         chosen by dropping one warp at a time until the shared memory fits,
+ *         and a resource error when even one warp does not fit.
+ */
+#ifndef HG_H_
+#define HG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t.  NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* hg_stream_t;
+
+typedef enum {
+    HG_OK = 0,
+    HG_ERR_INVALID_ARG = 1,       /* null pointer, negative size, misaligned pointer      */
+    HG_ERR_UNSUPPORTED_SHAPE = 2, /* K % 512 != 0, N % 128 != 0, or a size beyond limits  */
+    HG_ERR_RESOURCE = 3,          /* shared memory does not fit even the smallest block   */
+    HG_ERR_CUDA = 4,              /* a CUDA runtime / driver call failed                  */
+    HG_ERR_TIMEOUT = 5,           /* device: a bounded wait inside a kernel gave up        */
+    HG_ERR_BAD_OFFSETS = 6,       /* device: expert_offsets not monotone or beyond rows    */
+    HG_ERR_BAD_IDS = 7            /* device: an expert id outside [0, E) was dropped       */
+} hg_status;
+
+/* Static description of a status code.  Never NULL. */
+const char* hg_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int hg_version(void);
+
+/* ---------------------------------------------------------------- plan -- */
+
+/*
+ * Bytes of device workspace hg_plan_expert_offsets needs for M tokens with
+ * top_k experts each and E experts.  Pure function of its arguments (no
+ * device query).  Returns 0 for invalid arguments.
+ */
+size_t hg_plan_workspace_bytes(int32_t M, int32_t top_k, int32_t E);
+
+/*
+ * Threads per block the plan kernels use for E experts when a block may
+ * hold at most smem_limit_bytes of dynamic shared memory: the largest
+ * multiple of 32 not above 512 whose per-warp count table fits [M38,
+ * "修改方案"].  Returns 0 when not even 32 threads fit (the caller sees
+ * HG_ERR_RESOURCE from hg_plan_expert_offsets).  Host-only.
+ */
+int32_t hg_plan_block_threads(int32_t E, int32_t smem_limit_bytes);
+
+/*
+ * Routing plan [M38 background; H129 first section]: turn top-k expert ids
+ * into the grouped-contiguous row layout.
+ *
+ *   topk_ids        int32 [M, top_k], row-major; flat source index s = t*top_k + j.
+ *   expert_offsets  int32 [E+1] out: exclusive prefix sum of per-expert counts;
+ *                   expert e owns sorted rows [off[e], off[e+1]); off[E] = number
+ *                   of in-range ids (= M*top_k when all ids are in [0, E)).
+ *   sorted_to_src   int32 [M*top_k] out: source index s placed at each sorted
+ *                   row, ascending s inside an expert (stable); entries at and
+ *                   beyond off[E] are -1.
+ *   src_to_sorted   int32 [M*top_k] out: inverse permutation; -1 for an id
+ *                   outside [0, E).
+ *   workspace       device scratch of at least hg_plan_workspace_bytes(M, top_k, E)
+ *                   bytes (contents on entry ignored).
+ *
+ * Ids outside [0, E) are dropped from the layout and counted; the count is
+ * reported by hg_get_device_status as HG_ERR_BAD_IDS.  M = 0 writes zero
+ * offsets.  Results are bit-exact and deterministic.  Launches two kernels
+ * on `stream`; no host synchronisation.
+ */
+hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t E,
+                                 int32_t* expert_offsets, int32_t* sorted_to_src,
+                                 int32_t* src_to_sorted, void* workspace, size_t workspace_bytes,
+                                 hg_stream_t stream);
+
+/* ---------------------------------------------------------------- GEMM -- */
+
+/*
+ * Grouped-contiguous W4A8 GEMM [H129 benchmark command and first section]:
+ *
+ *   out[r, n] = bf16_rne( sum_k  A(r,k) * W(e(r), n, k) ),  e(r): off[e] <= r < off[e+1]
+ *   A(r,k)    = e4m3(a_fp8[r,k]) * 2^(a_scale[r, k/128] - 127)
+ *   W(e,n,k)  = e2m1(w_fp4[e,n,k]) * 2^(w_scale[e, n, k/32] - 127)
+ *
+ *   a_fp8      uint8 [rows, K]     E4M3 codes, row-major, rows sorted by expert;
+ *                                  16-byte aligned.
+ *   a_scale    uint8 [rows, K/128] E8M0 codes, one per row per 128-K group, row-major.
+ *   w_fp4      uint8 [E, N, K/2]   E2M1 codes, two per byte, element 2j in the low
+ *                                  nibble of byte j; 32-byte aligned.
+ *   w_scale    uint8 [E, N, K/32]  E8M0 codes, one per output column per 32-K group;
+ *                                  4-byte aligned.
+ *   expert_offsets int32 [E+1]     device array, e.g. from hg_plan_expert_offsets.
+ *   rows       number of rows of a_fp8 / a_scale / out (>= off[E]).
+ *   out_bf16   uint16 [rows, N]    bfloat16 bit patterns, row-major.  Rows at and
+ *                                  beyond off[E] are not written.
+ *
+ * Accumulation is FP32 inside the tensor cores; the scales are applied per
+ * 32-K block by the block-scaled MMA.  Supported: E in [1, 1024],
+ * N % 128 == 0, K % 512 == 0, rows in [0, 2^31).  Offsets that are not
+ * monotone or exceed rows are detected on the device: the affected experts
+ * are skipped and HG_ERR_BAD_OFFSETS is recorded for hg_get_device_status.
+ * E2M1/E4M3 NaN codes and E8M0 code 255 are not supported inputs.
+ * One persistent kernel launch on `stream`; no host synchronisation.
+ */
+hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
+                               const uint8_t* w_fp4, const uint8_t* w_scale,
+                               const int32_t* expert_offsets, int32_t E, int32_t N, int32_t K,
+                               int32_t rows, uint16_t* out_bf16, hg_stream_t stream);
+
+/* ------------------------------------------------------------- status -- */
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device: HG_OK, or the first device-side error recorded
+ * since the last call (HG_ERR_TIMEOUT, HG_ERR_BAD_OFFSETS, HG_ERR_BAD_IDS).
+ * If `detail` is not NULL it receives an error-specific value (for
+ * HG_ERR_BAD_IDS the number of dropped ids; for HG_ERR_TIMEOUT the role and
+ * stage of the wait that gave up).  Returns HG_ERR_CUDA if the stream or the
+ * context reports an error.
+ */
+hg_status hg_get_device_status(hg_stream_t stream, uint32_t* detail);
+
+/*
+ * Wait-timeout self test: launches one block that waits on a barrier nobody
+ * arrives at, through the same bounded wait the GEMM uses, with a limit of
+ * timeout_us microseconds.  The wait gives up, records HG_ERR_TIMEOUT in the
+ * status word and the kernel returns normally; the context stays usable.
+ */
+hg_status hg_selftest_wait_timeout(uint32_t timeout_us, hg_stream_t stream);
+
+/*
+ * Per-wait limit of the GEMM's barrier waits in microseconds (default
+ * 1000000).  Host-side setting, applied to later launches.  0 restores the
+ * default.
+ */
+void hg_set_wait_timeout_us(uint32_t timeout_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HG_H_ */

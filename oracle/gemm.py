@@ -99,3 +99,21 @@ def sampled_outputs(a_fp8, a_scale, w_fp4, w_scale, expert_offsets, rows_idx, co
                                 np.asarray(w_scale)[e[ok], n[ok]])
         vals[ok] = np.einsum("ik,ik->i", a_hat, w_hat)
     return round_f64_to_bf16_bits(vals)
+
+
+def rows_outputs(a_fp8, a_scale, w_fp4, w_scale, expert_offsets, rows_idx):
+    """BF16 bits of whole output rows out[r, :] for the sorted rows in rows_idx.
+
+    Groups the requested rows by expert and dequantises each touched
+    expert's weights once.  Rows that belong to no expert give +0.
+    """
+    r = np.asarray(rows_idx, dtype=np.int64)
+    e = expert_of_rows(expert_offsets, r)
+    N = np.asarray(w_fp4).shape[1]
+    vals = np.zeros((r.shape[0], N), dtype=np.float64)
+    for ee in np.unique(e[e >= 0]):
+        sel = np.nonzero(e == ee)[0]
+        a_hat = dequant_acts(np.asarray(a_fp8)[r[sel]], np.asarray(a_scale)[r[sel]])
+        w_hat = dequant_weights(np.asarray(w_fp4)[ee], np.asarray(w_scale)[ee])
+        vals[sel] = a_hat @ w_hat.T
+    return round_f64_to_bf16_bits(vals)

@@ -1,0 +1,111 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every function
+include/hg.h declares, and rejects bad arguments before any CUDA call.
+No compute calls are made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hg.h")
+LIB = os.path.join(ROOT, "fp8_mxfp4_grouped_gb300", "libhg.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from fp8_mxfp4_grouped_gb300 import build
+        build.build()
+    from fp8_mxfp4_grouped_gb300 import hg
+    return hg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("hg_plan_expert_offsets", "hg_grouped_w4a8_gemm", "hg_get_device_status",
+              "hg_plan_workspace_bytes", "hg_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\S+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        getattr(lib.lib, n)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.lib.hg_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.lib.hg_status_string(99) == b"unknown status"
+
+
+def test_plan_workspace_bytes(lib):
+    f = lib.hg_plan_workspace_bytes
+    assert f(16, 2, 4) == 1 * 4 * 4
+    assert f(16384, 8, 32) == 64 * 32 * 4
+    assert f(0, 8, 32) == 4 * 32
+    assert f(-1, 8, 32) == 0 and f(4, 0, 32) == 0 and f(4, 8, 0) == 0
+
+
+def test_plan_block_fit(lib):
+    # largest multiple of 32 <= 512 whose (warps + 2) x E x 4 bytes fit the limit
+    f = lib.hg_plan_block_threads
+    limit = 232448
+    prev = 512
+    for E in [1, 32, 512, 2048, 2880, 3072, 4608, 6144, 9216, 14000]:
+        t = f(E, limit)
+        assert t % 32 == 0 and 0 <= t <= 512
+        assert t <= prev
+        prev = t
+        if t:
+            assert (t // 32 + 2) * E * 4 <= limit
+            if t < 512:
+                assert ((t + 32) // 32 + 2) * E * 4 > limit
+    assert f(32, limit) == 512
+    assert f(20000, limit) == 0          # even one warp does not fit: resource error
+    assert f(0, limit) == 0 and f(32, 0) == 0
+
+
+def _gemm(lib, a=0x1000, asc=0x2000, w=0x4000, ws=0x8000, off=0x9000, E=4, N=256, K=512,
+          rows=32, out=0xA000):
+    c = ctypes.c_void_p
+    return lib.lib.hg_grouped_w4a8_gemm(c(a), c(asc), c(w), c(ws), c(off), E, N, K, rows, c(out),
+                                        None)
+
+
+def test_gemm_argument_validation(lib):
+    assert _gemm(lib, E=0) == lib.HG_ERR_INVALID_ARG
+    assert _gemm(lib, rows=-1) == lib.HG_ERR_INVALID_ARG
+    assert _gemm(lib, w=0) == lib.HG_ERR_INVALID_ARG
+    assert _gemm(lib, off=0) == lib.HG_ERR_INVALID_ARG
+    assert _gemm(lib, a=0) == lib.HG_ERR_INVALID_ARG
+    assert _gemm(lib, N=200) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, K=384) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, E=5000) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, w=0x4010) == lib.HG_ERR_INVALID_ARG      # W needs 32-byte alignment
+    assert _gemm(lib, a=0x1008) == lib.HG_ERR_INVALID_ARG      # A needs 16-byte alignment
+    assert _gemm(lib, ws=0x8001) == lib.HG_ERR_INVALID_ARG
+    # rows == 0 is a valid no-op that touches nothing
+    assert _gemm(lib, rows=0, a=0, asc=0, out=0) == lib.HG_OK
+
+
+def test_plan_argument_validation(lib):
+    c = ctypes.c_void_p
+    f = lib.lib.hg_plan_expert_offsets
+    assert f(c(0x1000), -1, 8, 32, c(0x2000), c(0x3000), c(0x4000), c(0x5000), 1 << 20, None) == lib.HG_ERR_INVALID_ARG
+    assert f(c(0x1000), 4, 0, 32, c(0x2000), c(0x3000), c(0x4000), c(0x5000), 1 << 20, None) == lib.HG_ERR_INVALID_ARG
+    assert f(c(0x1000), 4, 8, 32, None, c(0x3000), c(0x4000), c(0x5000), 1 << 20, None) == lib.HG_ERR_INVALID_ARG
+    assert f(c(0x1000), 4, 8, 32, c(0x2000), c(0x3000), c(0x4000), c(0x5000), 4, None) == lib.HG_ERR_INVALID_ARG
+    assert f(None, 4, 8, 32, c(0x2000), c(0x3000), c(0x4000), c(0x5000), 1 << 20, None) == lib.HG_ERR_INVALID_ARG

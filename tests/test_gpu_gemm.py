@@ -1,0 +1,267 @@
+"""Grouped W4A8 GEMM on the GPU vs the oracle.
+
+Small cases are compared element by element on the full output; the
+configurations' full sizes are compared on whole sampled rows (expert
+boundaries, token-tile boundaries, random rows) in the launch configuration
+the bench uses.  Tolerance: |gpu - ref| <= 1e-2 |ref| + 1e-2 rms(ref row).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gemm as G
+from oracle.plan import plan_expert_offsets
+from synth import make_case, make_routing
+from synth.inputs import CONFIGS, case_seed, make_acts, make_weights
+from tests.gpu_util import assert_rows_close, bf16_bits, np_u8
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_gemm(hg, a, a_s, w, w_s, off, out=None):
+    dev = "cuda"
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev).contiguous()
+    o = hg.hg_grouped_w4a8_gemm(t(a), t(a_s), t(w), t(w_s), t(np.asarray(off, dtype=np.int32)),
+                                out=out)
+    torch.cuda.synchronize()
+    return o
+
+
+def _pack(codes):
+    return (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+
+
+def _rand_codes(rng, R, K, E, N, scale_lo=120, scale_hi=134):
+    a = rng.integers(0, 256, (R, K), dtype=np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0x3C
+    a_s = rng.integers(scale_lo, scale_hi, (R, K // 128), dtype=np.uint8)
+    w = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    w_s = rng.integers(scale_lo, scale_hi, (E, N, K // 32), dtype=np.uint8)
+    return a, a_s, w, w_s
+
+
+def test_config0_full(cuda_lib):
+    c = make_case(0, 16)
+    ids = torch.from_numpy(c.topk_ids).cuda()
+    off_t, _, _ = cuda_lib.hg_plan_expert_offsets(ids, c.E)
+    out = cuda_lib.hg_grouped_w4a8_gemm(c.a_fp8.cuda(), c.a_scale.cuda(), c.w_fp4.cuda(),
+                                        c.w_scale.cuda(), off_t)
+    torch.cuda.synchronize()
+    off, *_ = plan_expert_offsets(c.topk_ids, c.E)
+    ref = G.grouped_w4a8_gemm(np_u8(c.a_fp8), np_u8(c.a_scale), np_u8(c.w_fp4), np_u8(c.w_scale),
+                              off, c.E, c.N, c.K)
+    assert_rows_close(bf16_bits(out), ref, "config 0")
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def test_identity_weights(cuda_lib):
+    # W = I per expert with unit scales: out = bf16(dequant(A)), exactly
+    rng = np.random.default_rng(1)
+    E, K = 2, 512
+    N = K
+    R = 40
+    a, a_s, _, _ = _rand_codes(rng, R, K, E, N)
+    codes = np.zeros((E, N, K), dtype=np.uint8)
+    for e in range(E):
+        codes[e, np.arange(N), np.arange(K)] = 0x2
+    w = _pack(codes)
+    w_s = np.full((E, N, K // 32), 127, dtype=np.uint8)
+    off = [0, 17, 40]
+    out = _run_gemm(cuda_lib, a, a_s, w, w_s, off)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, off, E, N, K)
+    g = bf16_bits(out)
+    from oracle.formats import bf16_bits_to_f64
+    assert np.array_equal(bf16_bits_to_f64(g), bf16_bits_to_f64(ref))
+
+
+def test_one_hot_weights_distinct_expert_scales(cuda_lib):
+    rng = np.random.default_rng(2)
+    E, N, K, R = 3, 256, 1024, 300
+    a, a_s, _, _ = _rand_codes(rng, R, K, E, N)
+    codes = np.zeros((E, N, K), dtype=np.uint8)
+    for e in range(E):
+        codes[e, np.arange(N), rng.permutation(K)[:N]] = 0x2
+    w = _pack(codes)
+    w_s = np.zeros((E, N, K // 32), dtype=np.uint8)
+    for e, c in enumerate([-2, 1, 4]):
+        w_s[e] = 127 + c
+    off = [0, 100, 130, 300]
+    out = _run_gemm(cuda_lib, a, a_s, w, w_s, off)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, off, E, N, K)
+    from oracle.formats import bf16_bits_to_f64
+    assert np.array_equal(bf16_bits_to_f64(bf16_bits(out)), bf16_bits_to_f64(ref))
+
+
+@pytest.mark.parametrize("E,N,K,cuts", [
+    (6, 384, 1024, [0, 1, 17, 17, 240, 470, 700]),        # 1-row, 16-row, empty, 1- and 2-tile experts
+    (3, 256, 2048, [0, 224, 225, 673]),                   # exactly one tile, one row, 3 tiles (448 + 1)
+    (4, 128, 512, [0, 0, 0, 33, 33]),                     # leading / trailing empty experts
+    (2, 512, 3072, [0, 129, 260]),                        # K = 24 stages: the ring wraps many times
+])
+def test_ragged_experts_random_codes(cuda_lib, E, N, K, cuts):
+    rng = np.random.default_rng(E * 1000 + K)
+    R = cuts[-1]
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    out = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K)
+    assert_rows_close(bf16_bits(out), ref, f"ragged E={E} N={N} K={K}")
+
+
+def test_wide_scale_range(cuda_lib):
+    rng = np.random.default_rng(5)
+    E, N, K, R = 2, 256, 1024, 70
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N, scale_lo=107, scale_hi=147)
+    off = [0, 31, 70]
+    out = _run_gemm(cuda_lib, a, a_s, w, w_s, off)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, off, E, N, K)
+    assert_rows_close(bf16_bits(out), ref, "wide scales")
+
+
+def test_guard_rows_untouched(cuda_lib):
+    # rows at and beyond off[E] belong to no expert and must not be written
+    rng = np.random.default_rng(6)
+    E, N, K, R = 3, 256, 512, 100
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    off = [0, 20, 50, 61]
+    out = torch.full((R, N), 12345.0, dtype=torch.bfloat16, device="cuda")
+    _run_gemm(cuda_lib, a, a_s, w, w_s, off, out=out)
+    canary = torch.tensor(12345.0, dtype=torch.bfloat16).view(torch.int16).item()
+    assert np.all(bf16_bits(out[61:]).view(np.int16) == canary)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, off, E, N, K)
+    assert_rows_close(bf16_bits(out[:61]), ref[:61], "guard")
+
+
+def test_deterministic(cuda_lib):
+    rng = np.random.default_rng(7)
+    E, N, K, R = 4, 512, 2048, 900
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    off = [0, 100, 400, 401, 900]
+    o1 = bf16_bits(_run_gemm(cuda_lib, a, a_s, w, w_s, off))
+    o2 = bf16_bits(_run_gemm(cuda_lib, a, a_s, w, w_s, off))
+    assert np.array_equal(o1, o2)
+
+
+def test_bad_offsets_reported(cuda_lib):
+    cuda_lib.hg_get_device_status()
+    rng = np.random.default_rng(8)
+    E, N, K, R = 3, 128, 512, 64
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    _run_gemm(cuda_lib, a, a_s, w, w_s, [0, 40, 20, 64])     # not monotone
+    st, _ = cuda_lib.hg_get_device_status()
+    assert st == cuda_lib.HG_ERR_BAD_OFFSETS
+    _run_gemm(cuda_lib, a, a_s, w, w_s, [0, 40, 50, 65])     # beyond rows
+    st, _ = cuda_lib.hg_get_device_status()
+    assert st == cuda_lib.HG_ERR_BAD_OFFSETS
+    # the context stays usable
+    off = [0, 10, 20, 64]
+    out = _run_gemm(cuda_lib, a, a_s, w, w_s, off)
+    assert_rows_close(bf16_bits(out), G.grouped_w4a8_gemm(a, a_s, w, w_s, off, E, N, K), "after")
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def test_wait_timeout_is_reported_and_context_survives(cuda_lib):
+    cuda_lib.hg_get_device_status()
+    cuda_lib.hg_selftest_wait_timeout(20000)        # 20 ms
+    st, detail = cuda_lib.hg_get_device_status()
+    assert st == cuda_lib.HG_ERR_TIMEOUT
+    assert (detail >> 24) == 6
+    test_config0_full(cuda_lib)
+
+
+# ------------------------------------------------ full-size sampled parity --
+
+def _sample_rows(off, rng, per_expert=3, max_experts=6):
+    """Expert boundaries, token-tile boundaries and random rows of a few experts."""
+    from fp8_mxfp4_grouped_gb300.tiles import token_tiles
+    off = np.asarray(off)
+    sizes = np.diff(off)
+    nz = np.nonzero(sizes)[0]
+    pick = set([int(nz[np.argmax(sizes[nz])]), int(nz[np.argmin(sizes[nz])])])
+    pick |= set(int(x) for x in rng.choice(nz, size=min(len(nz), max_experts - 2), replace=False))
+    rows = set()
+    for e in sorted(pick):
+        lo, hi = int(off[e]), int(off[e + 1])
+        rows |= {lo, hi - 1}
+        for r0, valid, _ in token_tiles(hi - lo):
+            rows |= {lo + r0, lo + r0 + valid - 1}
+        rows |= set(int(x) for x in rng.integers(lo, hi, per_expert))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+FULL_CASES = [(1, 64, None, None), (1, 2048, None, None), (2, 64, None, None),
+              (2, 16384, None, None), (3, 1, "w13", None), (3, 256, "w2", None),
+              (4, 4096, "gate_up", "uniform"), (4, 4096, "down", "biased")]
+
+
+@pytest.mark.parametrize("cid,M,proj,routing", FULL_CASES)
+def test_full_size_sampled_rows(cuda_lib, cid, M, proj, routing):
+    c = make_case(cid, M, projection=proj, routing=routing, device="cuda")
+    ids = torch.from_numpy(c.topk_ids).cuda()
+    off_t, _, _ = cuda_lib.hg_plan_expert_offsets(ids, c.E)
+    out = cuda_lib.hg_grouped_w4a8_gemm(c.a_fp8, c.a_scale, c.w_fp4, c.w_scale, off_t)
+    torch.cuda.synchronize()
+    off, *_ = plan_expert_offsets(c.topk_ids, c.E)
+    assert np.array_equal(off_t.cpu().numpy(), off)
+    rng = np.random.default_rng(cid * 100000 + M)
+    rows = _sample_rows(off, rng)
+    rr = torch.from_numpy(rows).cuda()
+    a = c.a_fp8[rr].cpu().numpy()
+    a_s = c.a_scale[rr].cpu().numpy()
+    # oracle on the sampled rows, re-indexed to a compact problem
+    e_of = G.expert_of_rows(off, rows)
+    experts = sorted(set(int(x) for x in e_of))
+    w = c.w_fp4[experts].cpu().numpy()
+    w_s = c.w_scale[experts].cpu().numpy()
+    local = np.array([experts.index(int(x)) for x in e_of])
+    order = np.argsort(local, kind="stable")
+    counts = np.bincount(local, minlength=len(experts))
+    loff = np.concatenate([[0], np.cumsum(counts)])
+    ref_sorted = G.grouped_w4a8_gemm(a[order], a_s[order], w, w_s, loff, len(experts), c.N, c.K)
+    ref = np.empty_like(ref_sorted)
+    ref[order] = ref_sorted
+    got = bf16_bits(out[rr])
+    assert_rows_close(got, ref, f"config {cid} M={M} {c.projection} {c.routing}", row_ids=rows)
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+@pytest.mark.parametrize("proj", ["w13", "w2"])
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_config3_small_m_full(cuda_lib, M, proj):
+    c = make_case(3, M, projection=proj)
+    ids = torch.from_numpy(c.topk_ids).cuda()
+    off_t, _, _ = cuda_lib.hg_plan_expert_offsets(ids, c.E)
+    out = cuda_lib.hg_grouped_w4a8_gemm(c.a_fp8.cuda(), c.a_scale.cuda(), c.w_fp4.cuda(),
+                                        c.w_scale.cuda(), off_t)
+    torch.cuda.synchronize()
+    off, *_ = plan_expert_offsets(c.topk_ids, c.E)
+    ref = G.grouped_w4a8_gemm(np_u8(c.a_fp8), np_u8(c.a_scale), np_u8(c.w_fp4),
+                              np_u8(c.w_scale), off, c.E, c.N, c.K)
+    assert_rows_close(bf16_bits(out), ref, f"config 3 M={M} {proj}")
+
+
+def test_graph_capture_replay_matches_eager(cuda_lib):
+    c = make_case(0, 16, device="cuda")
+    ids = torch.from_numpy(c.topk_ids).cuda()
+    E, R = c.E, c.R
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    s2d = torch.empty(R, dtype=torch.int32, device="cuda")
+    d2s = torch.empty(R, dtype=torch.int32, device="cuda")
+    ws = torch.empty(cuda_lib.hg_plan_workspace_bytes(16, 2, E), dtype=torch.uint8, device="cuda")
+    out = torch.empty((R, c.N), dtype=torch.bfloat16, device="cuda")
+    def step(stream):
+        cuda_lib.hg_plan_expert_offsets(ids, E, off, s2d, d2s, ws, stream=stream)
+        cuda_lib.hg_grouped_w4a8_gemm(c.a_fp8, c.a_scale, c.w_fp4, c.w_scale, off, out=out,
+                                      stream=stream)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(s)
+    torch.cuda.synchronize()
+    eager = bf16_bits(out).copy()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(out), eager)

@@ -1,0 +1,77 @@
+"""Routing plan on the GPU vs the oracle: bit-exact on every configuration's
+routing, plus edge cases (empty input, one expert, ids out of range, expert
+counts large enough to force a smaller block)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.plan import plan_expert_offsets
+from synth import make_routing
+from synth.inputs import CONFIGS, case_seed
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases():
+    out = []
+    for cid, cfg in CONFIGS.items():
+        for M in cfg["Ms"]:
+            for routing in cfg["routing"]:
+                out.append((cid, M, routing))
+    return out
+
+
+def _gpu_plan(hg, ids, E):
+    t = torch.from_numpy(np.ascontiguousarray(ids)).cuda()
+    off, s2d, d2s = hg.hg_plan_expert_offsets(t, E)
+    torch.cuda.synchronize()
+    return off.cpu().numpy(), s2d.cpu().numpy(), d2s.cpu().numpy()
+
+
+@pytest.mark.parametrize("cid,M,routing", _cases())
+def test_plan_matches_oracle(cuda_lib, cid, M, routing):
+    cfg = CONFIGS[cid]
+    E, k = cfg["E"], cfg["top_k"]
+    ids = make_routing(M, E, k, routing, case_seed(cid, M))
+    off, s2d, d2s = _gpu_plan(cuda_lib, ids, E)
+    r_off, r_s2d, r_d2s, bad = plan_expert_offsets(ids, E)
+    assert bad == 0
+    assert np.array_equal(off, r_off)
+    assert np.array_equal(s2d, r_s2d)
+    assert np.array_equal(d2s, r_d2s)
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+@pytest.mark.parametrize("M,k,E", [(1, 1, 1), (3, 2, 1), (37, 3, 5), (5000, 4, 7), (20000, 8, 64),
+                                   (4096, 8, 3000), (2000, 8, 6144)])
+def test_plan_random_shapes(cuda_lib, M, k, E):
+    rng = np.random.default_rng(M * 7 + E)
+    ids = rng.integers(0, E, (M, k)).astype(np.int32)     # duplicates allowed
+    off, s2d, d2s = _gpu_plan(cuda_lib, ids, E)
+    r_off, r_s2d, r_d2s, _ = plan_expert_offsets(ids, E)
+    assert np.array_equal(off, r_off) and np.array_equal(s2d, r_s2d) and np.array_equal(d2s, r_d2s)
+
+
+def test_plan_empty(cuda_lib):
+    t = torch.zeros((0, 8), dtype=torch.int32, device="cuda")
+    off, s2d, d2s = cuda_lib.hg_plan_expert_offsets(t, 4)
+    assert off.cpu().tolist() == [0] * 5
+
+
+def test_plan_out_of_range_ids(cuda_lib):
+    cuda_lib.hg_get_device_status()
+    ids = np.array([[0, 5], [-1, 1], [1, 0]] * 100, dtype=np.int32)
+    off, s2d, d2s = _gpu_plan(cuda_lib, ids, 2)
+    r_off, r_s2d, r_d2s, bad = plan_expert_offsets(ids, 2)
+    assert np.array_equal(off, r_off) and np.array_equal(s2d, r_s2d) and np.array_equal(d2s, r_d2s)
+    st, detail = cuda_lib.hg_get_device_status()
+    assert st == cuda_lib.HG_ERR_BAD_IDS and detail == bad == 200
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK     # read clears
+
+
+def test_plan_deterministic(cuda_lib):
+    ids = make_routing(16384, 32, 8, "biased", 7)
+    a = _gpu_plan(cuda_lib, ids, 32)
+    b = _gpu_plan(cuda_lib, ids, 32)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)

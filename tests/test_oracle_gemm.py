@@ -204,3 +204,15 @@ def test_sampled_outputs_equal_full_outputs():
 def test_expert_of_rows():
     off = np.array([0, 2, 2, 5], dtype=np.int32)
     assert G.expert_of_rows(off, [0, 1, 2, 3, 4, 5, 9]).tolist() == [0, 0, 2, 2, 2, -1, -1]
+
+
+def test_rows_outputs_equal_full_outputs():
+    rng = np.random.default_rng(15)
+    E, N, K, R = 4, 128, 512, 30
+    a, s = _rand_acts(rng, R, K)
+    w = _pack(rng.integers(0, 16, (E, N, K), dtype=np.uint8))
+    ws = rng.integers(120, 134, (E, N, K // 32), dtype=np.uint8)
+    off = np.array([0, 9, 9, 20, 27], dtype=np.int32)
+    full = G.grouped_w4a8_gemm(a, s, w, ws, off, E, N, K)
+    idx = np.array([29, 0, 8, 9, 19, 20, 26, 27, 3])
+    assert np.array_equal(G.rows_outputs(a, s, w, ws, off, idx), full[idx])
