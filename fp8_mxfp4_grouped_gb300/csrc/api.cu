@@ -31,6 +31,12 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_forced_variant{0};
+
+int choose_variant(int32_t E, int32_t rows) {
+    const int f = g_forced_variant.load();
+    return f ? f : gemm_pick_variant(E, rows);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -159,6 +165,7 @@ hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top
     a.threads = threads;
     a.nblk = nblk;
     a.chunk = static_cast<int>(chunk);
+    a.small = plan_small_fits(a.R, E, d->smem_optin);
     return launch_plan(a, s) == cudaSuccess ? HG_OK : HG_ERR_CUDA;
 }
 
@@ -178,14 +185,15 @@ hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
     DeviceInfo* d = nullptr;
     hg_status st = device_info(&d);
     if (st != HG_OK) return st;
-    if (static_cast<int>(gemm_smem_bytes(E)) > d->smem_optin) return HG_ERR_RESOURCE;
+    const int variant = choose_variant(E, rows);
+    if (static_cast<int>(gemm_smem_bytes(variant, E)) > d->smem_optin) return HG_ERR_RESOURCE;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     st = encoder(&encode);
     if (st != HG_OK) return st;
 
     // Weights: [E*N rows, K elements] of E2M1, unpacked by the TMA into one
     // 16-byte chunk (8 data bytes + 8 pad) per 16 elements, 128-byte swizzle.
-    CUtensorMap map_w, map_a;
+    CUtensorMap map_w, map_a, map_a64;
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
@@ -198,14 +206,15 @@ hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return HG_ERR_CUDA;
     }
-    // Activations: [rows, K] bytes, 16-row x 128-byte boxes, 128-byte swizzle.
-    {
+    // Activations: [rows, K] bytes, 128-byte swizzle; 16-row and 64-row boxes.
+    for (int which = 0; which < 2; ++which) {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-        cuuint32_t box[2] = {128, 16};
+        cuuint32_t box[2] = {128, which == 0 ? 16u : 64u};
         cuuint32_t estr[2] = {1, 1};
-        if (encode(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a_fp8), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        if (encode(which == 0 ? &map_a : &map_a64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<uint8_t*>(a_fp8), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return HG_ERR_CUDA;
@@ -224,7 +233,8 @@ hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
     a.status = d->status;
     a.timeout_ns = g_timeout_ns.load();
     a.num_sms = d->num_sms;
-    return launch_grouped_gemm(a, map_w, map_a, reinterpret_cast<cudaStream_t>(stream)) ==
+    a.variant = variant;
+    return launch_grouped_gemm(a, map_w, map_a, map_a64, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? HG_OK
                : HG_ERR_CUDA;
@@ -255,6 +265,16 @@ hg_status hg_selftest_wait_timeout(uint32_t timeout_us, hg_stream_t stream) {
                    cudaSuccess
                ? HG_OK
                : HG_ERR_CUDA;
+}
+
+int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows) {
+    if (E < 1 || N < 1 || K < 1 || rows < 0) return 0;
+    return gemm_variant_token_tile(choose_variant(E, rows));
+}
+
+int32_t hg_set_gemm_variant(int32_t variant) {
+    if (variant < 0 || variant > 3) return -1;
+    return g_forced_variant.exchange(variant);
 }
 
 void hg_set_wait_timeout_us(uint32_t timeout_us) {

@@ -16,8 +16,8 @@
 //  * one persistent CTA per SM walks a unit list (expert, weight-row tile,
 //    token tile) built on the device from expert_offsets; no host sync.
 //  * warp roles: warp 0 issues TMA loads (weights through the 16U4_ALIGN16B
-//    unpacking TMA type, activations as bytes; no multicast); warps 2,3,8,9
-//    stage the block scales into the tensor core's scale layout (activation
+//    unpacking TMA type, activations as bytes; no multicast) and L2
+//    prefetches several stages ahead; warps 2,3,8,9,10 stage the block scales into the tensor core's scale layout (activation
 //    scales are per 128-K, replicated into the four 32-K blocks they cover);
 //    warp 1 copies scales to TMEM and issues tcgen05.mma kind::mxf8f6f4 with
 //    block scaling, accumulating FP32 in TMEM; warps 4..7 drain the TMEM
@@ -33,37 +33,61 @@ namespace {
 
 constexpr int kBK = 128;              // K per pipeline stage = one activation-scale group
 constexpr int kBW = 128;              // weight rows per tile (MMA M)
-constexpr int kTMax = 224;            // largest token tile (MMA N), multiple of 16
-constexpr int kStages = 4;
-constexpr int kSfWarps = 4;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 320;         // 10 warps
-constexpr int kABoxRows = 16;         // rows per activation TMA box
-constexpr int kMaxE = 1024;
-
+constexpr int kABoxRows = 16;         // rows per small activation TMA box
+constexpr int kABigRows = 64;         // rows per large activation TMA box
+constexpr int kMaxE = 512;            // scheduler tables live in shared memory
 constexpr uint32_t kWTileBytes = kBW * kBK;    // unpacked E2M1: one byte of smem per element
 // The 16U4_ALIGN16B TMA load writes 8 data bytes into each 16-byte chunk and
 // leaves the other 8 untouched; its transaction count is the packed bytes.
 constexpr uint32_t kWTileTx = kBW * kBK / 2;
-constexpr uint32_t kATileBytes = kTMax * kBK;
 constexpr uint32_t kABoxBytes = kABoxRows * kBK;
+constexpr uint32_t kABigBytes = kABigRows * kBK;
 constexpr uint32_t kSfaBytes = 512;            // 128 rows x 4 blocks of 32 K
-constexpr uint32_t kSfbBytes = 1024;           // up to 256 tokens x 4 blocks
-constexpr uint32_t kAccCols = kTMax;           // TMEM columns per accumulator buffer
-constexpr uint32_t kSfCol0 = 2 * kAccCols;     // scale factors after both accumulators
-constexpr uint32_t kSfSlotCols = 12;           // 4 (weights) + 8 (tokens) per stage
-constexpr uint32_t kTmemCols = 512;
-static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "TMEM budget");
-static_assert(kSfWarps == kStages, "one scale warp per ring slot");
+constexpr uint32_t kSmemPerSm = 233472;        // 228 KB per SM on sm_103
+constexpr uint32_t kSmemPerBlockMax = 232448;  // 227 KB opt-in per block
+constexpr uint32_t kSmemReservedPerBlock = 1024;
 
-constexpr uint32_t kOffW = 0;
-constexpr uint32_t kOffA = kOffW + kStages * kWTileBytes;
-constexpr uint32_t kOffSfa = kOffA + kStages * kATileBytes;
-constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr uint32_t kOffMisc = kOffBar + 256;
-constexpr uint32_t kOffSched = kOffMisc + 64;
-static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
+// One pipeline shape.  T: largest token tile (MMA N); S: ring stages; C: CTAs
+// resident per SM.  Each CTA is a complete pipeline; with C = 2 two MMA
+// issuers share the SM's tensor core (one thread issues one MMA per ~80-130
+// cycles, so small tiles need two issuers to keep up with HBM).
+template <int T, int S, int C>
+struct GemmCfg {
+    static constexpr int kTMax = T;
+    static constexpr int kStages = S;
+    static constexpr int kCtasPerSm = C;
+    static constexpr int kSfWarps = S;                     // one scale warp per ring slot
+    static constexpr int kThreads = 32 * (6 + S);          // TMA, MMA, 4 epilogue, S scale warps
+    static constexpr uint32_t kATileBytes = T * kBK;
+    static constexpr int kSfbAtoms = T > 128 ? 2 : 1;      // 128 tokens per scale block
+    static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
+    static constexpr uint32_t kAccCols = T;                // TMEM columns per accumulator
+    static constexpr uint32_t kTmemCols = 512 / C;
+    static constexpr uint32_t kSfCol0 = 2 * kAccCols;      // scale slots after both accumulators
+    static constexpr uint32_t kSfSlotCols = 4 + 4 * kSfbAtoms;
+    static constexpr uint32_t kOffW = 0;
+    static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
+    static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
+    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;
+    static constexpr uint32_t kOffBar = kOffSfb + S * kSfbBytes;
+    static constexpr uint32_t kOffMisc = kOffBar + 256;
+    static constexpr uint32_t kOffSched = kOffMisc + 64;
+    static constexpr size_t smem_bytes(int E) {
+        return kOffSched + static_cast<size_t>(5 * E + 1) * sizeof(int32_t) + 1024;
+    }
+    static constexpr size_t kSmemBudget =
+        C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
+    static_assert(T % 16 == 0 && T >= 16 && T <= 256, "MMA N");
+    static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
+    static_assert(kSfCol0 + S * kSfSlotCols <= kTmemCols, "TMEM budget");
+    static_assert(smem_bytes(kMaxE) <= kSmemBudget, "shared memory budget");
+    static_assert(C * 32 * (6 + S) * 96 <= 65536, "registers for C resident CTAs");
+};
+
+using CfgSmall = GemmCfg<64, 4, 2>;    // few rows per expert: HBM-bound weight streaming
+using CfgMid = GemmCfg<112, 3, 2>;     // a few hundred rows per expert
+using CfgLarge = GemmCfg<224, 4, 1>;   // many rows per expert: tensor-bound
 
 struct Sched {
     const int32_t* start;
@@ -124,12 +148,16 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
 grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_a64,
                     const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
                     const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
                     uint16_t* __restrict__ out, uint32_t* status, uint64_t timeout_ns) {
+    constexpr int kStages = Cfg::kStages;
+    constexpr int kTMax = Cfg::kTMax;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -138,14 +166,14 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const uint32_t bar_full_tma = sbase + kOffBar;
+    const uint32_t bar_full_tma = sbase + Cfg::kOffBar;
     const uint32_t bar_full_sf = bar_full_tma + 8 * kStages;
     const uint32_t bar_empty = bar_full_sf + 8 * kStages;
     const uint32_t bar_tfull = bar_empty + 8 * kStages;
     const uint32_t bar_tempty = bar_tfull + 16;
     const uint32_t bar_done = bar_tempty + 16;
-    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
-    int32_t* s_start = reinterpret_cast<int32_t*>(base + kOffSched);
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(base + Cfg::kOffMisc);
+    int32_t* s_start = reinterpret_cast<int32_t*>(base + Cfg::kOffSched);
     int32_t* s_rows = s_start + E;
     int32_t* s_ntt = s_rows + E;
     int32_t* s_tile = s_ntt + E;
@@ -166,17 +194,18 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         ptx::fence_barrier_init();
     }
     if (warp == 1) {
-        ptx::tmem_alloc(sbase + kOffMisc, kTmemCols);
+        ptx::tmem_alloc(sbase + Cfg::kOffMisc, Cfg::kTmemCols);
         ptx::tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&map_w);
         ptx::prefetch_tensormap(&map_a);
+        ptx::prefetch_tensormap(&map_a64);
     }
 
     // Per-expert token tiling, from the expert's own row count.
     const int NT = N / kBW;
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+    for (int e = threadIdx.x; e < E; e += Cfg::kThreads) {
         const int lo = offsets[e];
         const int hi = offsets[e + 1];
         int r = 0;
@@ -230,6 +259,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
                 const Unit t = decode_unit(sch, u);
                 const int wrow = t.e * N + t.n0;
+                const int nbig = t.n_mma / kABigRows;
+                const int nsmall = (t.n_mma - nbig * kABigRows) / kABoxRows;
                 for (int ks = 0; ks < KT; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
@@ -239,12 +270,17 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     }
                     const uint32_t fb = bar_full_tma + 8 * slot;
                     ptx::mbar_arrive_expect_tx(fb, kWTileTx + t.n_mma * kBK);
-                    ptx::tma_load_2d(sbase + kOffW + slot * kWTileBytes, &map_w, ks * kBK, wrow, fb,
-                                     pol_w);
-                    const uint32_t adst = sbase + kOffA + slot * kATileBytes;
-                    for (int j = 0; j < t.n_mma / kABoxRows; ++j) {
-                        ptx::tma_load_2d(adst + j * kABoxBytes, &map_a, ks * kBK,
-                                         t.row0 + j * kABoxRows, fb, pol_a);
+                    ptx::tma_load_2d(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w, ks * kBK,
+                                     wrow, fb, pol_w);
+                    const uint32_t adst = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
+                    for (int j = 0; j < nbig; ++j) {
+                        ptx::tma_load_2d(adst + j * kABigBytes, &map_a64, ks * kBK,
+                                         t.row0 + j * kABigRows, fb, pol_a);
+                    }
+                    const int r0 = nbig * kABigRows;
+                    for (int j = 0; j < nsmall; ++j) {
+                        ptx::tma_load_2d(adst + (r0 + j * kABoxRows) * kBK, &map_a, ks * kBK,
+                                         t.row0 + r0 + j * kABoxRows, fb, pol_a);
                     }
                 }
             }
@@ -270,7 +306,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 ptx::tc_fence_after();
                 const uint32_t idesc0 =
                     ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, kBW, t.n_mma);
-                const uint32_t d_tmem = tmem_base + b * kAccCols;
+                const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
                 for (int ks = 0; ks < KT; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
@@ -280,16 +316,16 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sf_col = tmem_base + kSfCol0 + slot * kSfSlotCols;
-                    const uint32_t sfa = sbase + kOffSfa + slot * kSfaBytes;
-                    const uint32_t sfb = sbase + kOffSfb + slot * kSfbBytes;
+                    const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
+                    const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
+                    const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
                     ptx::tc_cp_32x128b_warpx4(sf_col, ptx::desc_sf_32x16(sfa));
                     ptx::tc_cp_32x128b_warpx4(sf_col + 4, ptx::desc_sf_32x16(sfb));
-                    if (t.n_mma > 128) {
+                    if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
                         ptx::tc_cp_32x128b_warpx4(sf_col + 8, ptx::desc_sf_32x16(sfb + 512));
                     }
-                    const uint32_t wsm = sbase + kOffW + slot * kWTileBytes;
-                    const uint32_t asm_ = sbase + kOffA + slot * kATileBytes;
+                    const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
+                    const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk) {
                         ptx::mma_mxf8f6f4_1x(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
@@ -317,7 +353,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             ptx::tc_fence_after();
             const int n = t.n0 + 32 * q + lane;
             uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kAccCols;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
             for (int c0 = 0; c0 < t.nrows; c0 += 16) {
                 uint32_t v[16];
                 ptx::tmem_ld_32x32b_x16(taddr + c0, v);
@@ -336,7 +373,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         }
     } else {
         // ------------------------------------------- scale staging -----
-        const int sfw = (warp == 2) ? 0 : (warp == 3) ? 1 : (warp == 8) ? 2 : 3;
+        const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;   // warps 2, 3, 8, 9, ...
         const int ws_row = K / 32;     // bytes per w_scale row
         const int as_row = K / kBK;    // bytes per a_scale row
         uint32_t g = 0;
@@ -345,7 +382,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             const Unit t = decode_unit(sch, u);
             const uint8_t* wsrc = w_scale + static_cast<size_t>(t.e * N + t.n0 + lane) * ws_row;
             for (int ks = 0; ks < KT; ++ks, ++g) {
-                if (static_cast<int>(g % kSfWarps) != sfw) continue;
+                if (static_cast<int>(g % Cfg::kSfWarps) != sfw) continue;
                 const uint32_t slot = g % kStages;
                 const uint32_t ph = (g / kStages) & 1u;
                 // Weight scales: row n = lane + 32c, the four 32-K blocks of
@@ -357,9 +394,9 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 }
                 // Token scales: one per 128-K group, replicated into the four
                 // 32-K blocks.  Token index = 128a + lane + 32c.
-                uint32_t av[8];
+                uint32_t av[4 * Cfg::kSfbAtoms];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4 * Cfg::kSfbAtoms; ++i) {
                     const int tok = 128 * (i >> 2) + lane + 32 * (i & 3);
                     const int r = t.row0 + tok;
                     av[i] = 0x7F7F7F7Fu;
@@ -373,11 +410,14 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     ok = false;
                     break;
                 }
-                const uint32_t sfa = sbase + kOffSfa + slot * kSfaBytes + 16 * lane;
-                const uint32_t sfb = sbase + kOffSfb + slot * kSfbBytes + 16 * lane;
+                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes + 16 * lane;
+                const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes + 16 * lane;
                 sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
                 sts_v4(sfb, av[0], av[1], av[2], av[3]);
-                if (t.n_mma > 128) sts_v4(sfb + 512, av[4], av[5], av[6], av[7]);
+                if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
+                    sts_v4(sfb + 512, av[4 % (4 * Cfg::kSfbAtoms)], av[5 % (4 * Cfg::kSfbAtoms)],
+                           av[6 % (4 * Cfg::kSfbAtoms)], av[7 % (4 * Cfg::kSfbAtoms)]);
+                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar_full_sf + 8 * slot);
@@ -389,7 +429,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, kTmemCols);
+        ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
 }
 
@@ -411,37 +451,70 @@ __global__ void selftest_wait_kernel(uint32_t* status, uint64_t timeout_ns) {
     __syncthreads();
 }
 
-}  // namespace
-
-size_t gemm_smem_bytes(int32_t E) {
-    return kOffSched + static_cast<size_t>(5 * E + 1) * sizeof(int32_t) + 1024;
+template <class Cfg>
+cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
+                       const CUtensorMap& map_a64, cudaStream_t stream) {
+    static bool configured = false;   // the attribute is per kernel, process-wide
+    if (!configured) {
+        cudaError_t err = cudaFuncSetAttribute(grouped_w4a8_kernel<Cfg>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(Cfg::smem_bytes(kMaxE)));
+        if (err != cudaSuccess) return err;
+        configured = true;
+    }
+    // Upper bound on the number of units: every non-empty expert needs at
+    // most ceil(rows_e / T) token tiles <= rows_e / T + 1.
+    const long long nt = a.N / kBW;
+    const long long active = a.E < a.rows ? a.E : a.rows;
+    const long long units_max = ((a.rows + Cfg::kTMax - 1) / Cfg::kTMax + active) * nt;
+    long long grid = static_cast<long long>(a.num_sms) * Cfg::kCtasPerSm;
+    if (units_max < grid) grid = units_max;
+    if (grid < 1) return cudaSuccess;
+    grouped_w4a8_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
+                               stream>>>(map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets,
+                                         a.E, a.N, a.K, a.rows, a.out, a.status, a.timeout_ns);
+    return cudaGetLastError();
 }
+
+}  // namespace
 
 int gemm_max_experts() { return kMaxE; }
 
-cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
-                                const CUtensorMap& map_a, cudaStream_t stream) {
-    const size_t smem = gemm_smem_bytes(a.E);
-    static int configured_smem = 0;   // the attribute is per function, process-wide
-    if (static_cast<int>(smem) > configured_smem) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_w4a8_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(gemm_smem_bytes(kMaxE)));
-        if (err != cudaSuccess) return err;
-        configured_smem = static_cast<int>(gemm_smem_bytes(kMaxE));
+// Variant choice from the mean rows per expert (the per-expert counts live on
+// the device).  Few rows: weight streaming dominates and two small pipelines
+// per SM keep the MMA issue rate up; many rows: the widest token tile.
+int gemm_pick_variant(int32_t E, int32_t rows) {
+    const long long per = rows / (E > 0 ? E : 1);
+    if (per <= 48) return 1;
+    if (per <= 640) return 2;
+    return 3;
+}
+
+int gemm_variant_token_tile(int variant) {
+    switch (variant) {
+        case 1: return CfgSmall::kTMax;
+        case 2: return CfgMid::kTMax;
+        case 3: return CfgLarge::kTMax;
+        default: return 0;
     }
-    // Upper bound on the number of units: every non-empty expert needs at
-    // most ceil(rows_e / kTMax) token tiles <= rows_e / kTMax + 1.
-    const long long nt = a.N / kBW;
-    const long long active = a.E < a.rows ? a.E : a.rows;
-    const long long units_max = ((a.rows + kTMax - 1) / kTMax + active) * nt;
-    int grid = a.num_sms;
-    if (units_max < grid) grid = static_cast<int>(units_max);
-    if (grid < 1) return cudaSuccess;
-    grouped_w4a8_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_a, a.a_scale, a.w_scale,
-                                                           a.offsets, a.E, a.N, a.K, a.rows, a.out,
-                                                           a.status, a.timeout_ns);
-    return cudaGetLastError();
+}
+
+size_t gemm_smem_bytes(int variant, int32_t E) {
+    switch (variant) {
+        case 1: return CfgSmall::smem_bytes(E);
+        case 2: return CfgMid::smem_bytes(E);
+        default: return CfgLarge::smem_bytes(E);
+    }
+}
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
+                                const CUtensorMap& map_a, const CUtensorMap& map_a64,
+                                cudaStream_t stream) {
+    switch (a.variant) {
+        case 1: return launch_cfg<CfgSmall>(a, map_w, map_a, map_a64, stream);
+        case 2: return launch_cfg<CfgMid>(a, map_w, map_a, map_a64, stream);
+        default: return launch_cfg<CfgLarge>(a, map_w, map_a, map_a64, stream);
+    }
 }
 
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream) {

@@ -73,12 +73,16 @@ struct GemmArgs {
     uint32_t* status;
     uint64_t timeout_ns;
     int num_sms;
+    int variant;   // 1 small tiles / 2 CTAs per SM, 2 mid, 3 large tiles / 1 CTA per SM
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
-                                const CUtensorMap& map_a, cudaStream_t stream);
-size_t gemm_smem_bytes(int32_t E);
+                                const CUtensorMap& map_a, const CUtensorMap& map_a64,
+                                cudaStream_t stream);
+size_t gemm_smem_bytes(int variant, int32_t E);
 int gemm_max_experts();
+int gemm_pick_variant(int32_t E, int32_t rows);
+int gemm_variant_token_tile(int variant);
 
 struct PlanArgs {
     const int32_t* ids;
@@ -91,10 +95,12 @@ struct PlanArgs {
     int threads;   // block size chosen by the shared-memory fit
     int nblk;      // number of blocks of the histogram / scatter grids
     int chunk;     // ids per block (multiple of 32)
+    bool small;    // whole plan in one 1024-thread block (plan_small_fits)
 };
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 size_t plan_smem_bytes(int32_t E, int threads);
+bool plan_small_fits(int32_t R, int32_t E, int smem_limit);
 
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 

@@ -8,7 +8,10 @@
 // contiguous one of humming PR #129 ("perf(sm90): size grouped W4A8 tiles
 // per expert", first section): each expert's rows form one range.
 //
-// Two launches:
+// Up to 6144 routed rows (and E small enough for a 32-warp count table) the
+// whole plan is ONE block of 1024 threads (plan_small): each warp keeps its
+// contiguous sub-chunk of ids in registers, counts it, and after one scan
+// places it.  Larger inputs take two launches:
 //   plan_hist:    block b counts the ids of its chunk per expert
 //                 (warp-aggregated with __match_any_sync) -> ws[b][e].
 //   plan_scatter: every block rebuilds the exclusive scan over (expert,
@@ -169,13 +172,153 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ ids, int R, int 
     }
 }
 
+
+#ifndef HG_PLAN_SMALL_MAX_R
+#define HG_PLAN_SMALL_MAX_R 6144
+#endif
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallIdsPerLane = 16;
+constexpr int kSmallMaxR = HG_PLAN_SMALL_MAX_R;
+static_assert(kSmallMaxR <= kSmallThreads * kSmallIdsPerLane, "ids must fit the registers");
+
+// Shared memory: per-warp table wc[32][E], base[E], then the permutation
+// sorted_to_src itself (R entries): placing rows in shared memory and writing
+// the array out once, coalesced, avoids R scattered 4-byte global stores
+// from a single SM.
+__global__ void __launch_bounds__(kSmallThreads)
+plan_small_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ sorted_to_src, int32_t* __restrict__ src_to_sorted,
+                  uint32_t* status) {
+    extern __shared__ int32_t sm_small[];
+    constexpr int nw = kSmallThreads / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int32_t* wc = sm_small;                        // [nw][E]
+    int32_t* base = wc + nw * E;                   // [E]
+    int32_t* s2d = base + E;                       // [R]
+    __shared__ int32_t s_total;
+
+    // Contiguous sub-chunk per warp, a multiple of 32 ids long.
+    const int sub = ((R + nw - 1) / nw + 31) & ~31;
+    const int wbeg = warp * sub;
+    const int wend = min(R, wbeg + sub);
+    int key[kSmallIdsPerLane];
+#pragma unroll
+    for (int j = 0; j < kSmallIdsPerLane; ++j) {
+        const int i = wbeg + 32 * j + lane;
+        key[j] = -2;
+        if (32 * j < sub && i < wend) {
+            const int e = __ldg(ids + i);
+            key[j] = (e >= 0 && e < E) ? e : -1;
+        }
+    }
+    for (int i = threadIdx.x; i < (nw + 1) * E; i += kSmallThreads) sm_small[i] = 0;
+    __syncthreads();
+
+    int32_t* mycnt = wc + warp * E;
+    uint32_t bad = 0;
+#pragma unroll
+    for (int j = 0; j < kSmallIdsPerLane; ++j) {
+        if (32 * j < sub) {
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key[j]);
+            if (key[j] >= 0 && lane == __ffs(peers) - 1) mycnt[key[j]] += __popc(peers);
+            if (key[j] == -1) ++bad;
+        }
+    }
+    if (bad) {
+        atomicAdd(&status[kStatusBadIds], bad);
+        record_error(status, HG_ERR_BAD_IDS, 0u);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kSmallThreads) {
+        int t = 0;
+        for (int w = 0; w < nw; ++w) t += wc[w * E + e];
+        base[e] = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int c = 0; c < E; c += 32) {
+            const int e = c + lane;
+            const int v = e < E ? base[e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (e < E) {
+                offsets[e] = carry + incl - v;
+                base[e] = carry + incl - v;
+            }
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) {
+            offsets[E] = carry;
+            s_total = carry;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kSmallThreads) {
+        int run = base[e];
+        for (int w = 0; w < nw; ++w) {
+            const int c = wc[w * E + e];
+            wc[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < kSmallIdsPerLane; ++j) {
+        if (32 * j < sub) {
+            const int i = wbeg + 32 * j + lane;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key[j]);
+            int dest = -1;
+            if (key[j] >= 0) dest = mycnt[key[j]] + __popc(peers & lt);
+            __syncwarp();
+            if (key[j] >= 0 && lane == __ffs(peers) - 1) mycnt[key[j]] += __popc(peers);
+            __syncwarp();
+            if (i < wend) {
+                src_to_sorted[i] = dest;
+                if (dest >= 0) s2d[dest] = i;
+            }
+        }
+    }
+    __syncthreads();
+    const int total = s_total;
+    for (int j = threadIdx.x; j < R; j += kSmallThreads) sorted_to_src[j] = j < total ? s2d[j] : -1;
+}
+
 }  // namespace
+
+size_t plan_small_smem_bytes(int32_t R, int32_t E) {
+    return (static_cast<size_t>(kSmallThreads / 32 + 1) * static_cast<size_t>(E) +
+            static_cast<size_t>(R)) * sizeof(int32_t);
+}
+
+bool plan_small_fits(int32_t R, int32_t E, int smem_limit) {
+    return R <= kSmallMaxR && plan_small_smem_bytes(R, E) <= static_cast<size_t>(smem_limit);
+}
 
 size_t plan_smem_bytes(int32_t E, int threads) {
     return static_cast<size_t>(threads / 32 + 2) * static_cast<size_t>(E) * sizeof(int32_t);
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
+    if (a.small) {
+        const size_t smem = plan_small_smem_bytes(a.R, a.E);
+        if (smem > 48 * 1024) {
+            cudaError_t err = cudaFuncSetAttribute(plan_small_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+            if (err != cudaSuccess) return err;
+        }
+        plan_small_kernel<<<1, kSmallThreads, smem, stream>>>(a.ids, a.R, a.E, a.offsets,
+                                                               a.sorted_to_src, a.src_to_sorted,
+                                                               a.status);
+        return cudaGetLastError();
+    }
     const size_t smem_hist = static_cast<size_t>(a.E) * sizeof(int32_t);
     const size_t smem_scat = plan_smem_bytes(a.E, a.threads);
     if (smem_scat > 48 * 1024) {

@@ -45,6 +45,10 @@ lib.hg_selftest_wait_timeout.argtypes = [_u32, _p]
 lib.hg_selftest_wait_timeout.restype = ctypes.c_int
 lib.hg_set_wait_timeout_us.argtypes = [_u32]
 lib.hg_set_wait_timeout_us.restype = None
+lib.hg_gemm_token_tile.argtypes = [_i32, _i32, _i32, _i32]
+lib.hg_gemm_token_tile.restype = _i32
+lib.hg_set_gemm_variant.argtypes = [_i32]
+lib.hg_set_gemm_variant.restype = _i32
 
 HG_OK = 0
 HG_ERR_INVALID_ARG = 1
@@ -142,3 +146,14 @@ def hg_selftest_wait_timeout(timeout_us: int, stream=None):
 
 def hg_set_wait_timeout_us(timeout_us: int):
     lib.hg_set_wait_timeout_us(timeout_us)
+
+
+def hg_gemm_token_tile(E: int, N: int, K: int, rows: int) -> int:
+    return int(lib.hg_gemm_token_tile(E, N, K, rows))
+
+
+def hg_set_gemm_variant(variant: int) -> int:
+    prev = int(lib.hg_set_gemm_variant(variant))
+    if prev < 0:
+        raise ValueError(f"invalid GEMM variant {variant}")
+    return prev

@@ -13,29 +13,41 @@ tcgen05 kernel where an expert's tokens are the MMA's N side:
     tile(e) = round_up_16(ceil(rows_e / n_t(e)))      rows per token tile
     the last tile of an expert issues MMA N = round_up_16(rows left)
 
-With T_MAX = 224 an expert with 130 rows takes one 144-column tile where a
-fixed 128-row tile would take two.
+T_MAX depends on the pipeline variant the library picks from rows / E
+(``hg_gemm_token_tile``): 64, 112 or 224.  With T_MAX = 224 an expert with
+130 rows takes one 144-column tile where a fixed 128-row tile would take two.
 """
 from __future__ import annotations
 
 T_MAX = 224
+VARIANT_T_MAX = {1: 64, 2: 112, 3: 224}
 MMA_N_STEP = 16
 W_TILE = 128
 
 
-def expert_tiling(rows_e: int):
+def pick_variant(E: int, rows: int) -> int:
+    """Mirror of the library's variant choice (mean rows per expert)."""
+    per = rows // max(E, 1)
+    if per <= 48:
+        return 1
+    if per <= 640:
+        return 2
+    return 3
+
+
+def expert_tiling(rows_e: int, t_max: int = T_MAX):
     """(n_t, tile) for one expert; (0, 0) for an empty expert."""
     if rows_e <= 0:
         return 0, 0
-    n_t = -(-rows_e // T_MAX)
+    n_t = -(-rows_e // t_max)
     per = -(-rows_e // n_t)
     tile = -(-per // MMA_N_STEP) * MMA_N_STEP
     return n_t, tile
 
 
-def token_tiles(rows_e: int):
+def token_tiles(rows_e: int, t_max: int = T_MAX):
     """List of (first_row, valid_rows, mma_n) of one expert's token tiles."""
-    n_t, tile = expert_tiling(rows_e)
+    n_t, tile = expert_tiling(rows_e, t_max)
     out = []
     for tt in range(n_t):
         r0 = tt * tile
@@ -44,13 +56,13 @@ def token_tiles(rows_e: int):
     return out
 
 
-def units(offsets, N: int):
+def units(offsets, N: int, t_max: int = T_MAX):
     """Work units of one launch: (expert, n0, first sorted row, valid rows, mma_n)."""
     E = len(offsets) - 1
     out = []
     for e in range(E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
-        tiles = token_tiles(hi - lo)
+        tiles = token_tiles(hi - lo, t_max)
         for nt in range(N // W_TILE):
             for (r0, valid, mma_n) in tiles:
                 out.append((e, nt * W_TILE, lo + r0, valid, mma_n))

@@ -89,8 +89,9 @@ int32_t hg_plan_block_threads(int32_t E, int32_t smem_limit_bytes);
  *
  * Ids outside [0, E) are dropped from the layout and counted; the count is
  * reported by hg_get_device_status as HG_ERR_BAD_IDS.  M = 0 writes zero
- * offsets.  Results are bit-exact and deterministic.  Launches two kernels
- * on `stream`; no host synchronisation.
+ * offsets.  Results are bit-exact and deterministic.  Up to 6144 routed
+ * rows the plan is one single-block kernel; beyond that, two kernels.
+ * Launches on `stream`; no host synchronisation.
  */
 hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t E,
                                  int32_t* expert_offsets, int32_t* sorted_to_src,
@@ -119,17 +120,36 @@ hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top
  *                                  beyond off[E] are not written.
  *
  * Accumulation is FP32 inside the tensor cores; the scales are applied per
- * 32-K block by the block-scaled MMA.  Supported: E in [1, 1024],
+ * 32-K block by the block-scaled MMA.  Supported: E in [1, 512],
  * N % 128 == 0, K % 512 == 0, rows in [0, 2^31).  Offsets that are not
  * monotone or exceed rows are detected on the device: the affected experts
  * are skipped and HG_ERR_BAD_OFFSETS is recorded for hg_get_device_status.
  * E2M1/E4M3 NaN codes and E8M0 code 255 are not supported inputs.
- * One persistent kernel launch on `stream`; no host synchronisation.
+ * One persistent kernel launch on `stream`; no host synchronisation.  The
+ * pipeline shape (largest token tile, CTAs per SM) is chosen from the mean
+ * rows per expert, rows / E; results do not depend on the choice beyond the
+ * FP32 summation order inside one output element, which is the same for all.
  */
 hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
                                const uint8_t* w_fp4, const uint8_t* w_scale,
                                const int32_t* expert_offsets, int32_t E, int32_t N, int32_t K,
                                int32_t rows, uint16_t* out_bf16, hg_stream_t stream);
+
+/*
+ * Largest token tile (MMA N) hg_grouped_w4a8_gemm uses for these arguments:
+ * an expert with r rows is cut into ceil(r / T) tiles of equal size rounded
+ * up to 16 rows.  Host-only query; 0 for invalid arguments.
+ */
+int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows);
+
+/*
+ * Force the GEMM pipeline variant for later calls in this process: 0 = choose
+ * automatically (default), 1 = 64-row token tiles with two CTAs per SM,
+ * 2 = 112-row tiles with two CTAs per SM, 3 = 224-row tiles with one CTA per
+ * SM.  Meant for tests and tuning.  Returns the previous setting, or -1 for
+ * an invalid value (setting unchanged).  Host-only.
+ */
+int32_t hg_set_gemm_variant(int32_t variant);
 
 /* ------------------------------------------------------------- status -- */
 

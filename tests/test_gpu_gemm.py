@@ -17,6 +17,15 @@ from tests.gpu_util import assert_rows_close, bf16_bits, np_u8
 
 pytestmark = pytest.mark.gpu
 
+VARIANTS = [1, 2, 3]   # 64-row / 112-row tiles with 2 CTAs per SM, 224-row tiles with 1
+
+
+@pytest.fixture(params=VARIANTS, ids=lambda v: f"variant{v}")
+def variant(request, cuda_lib):
+    prev = cuda_lib.hg_set_gemm_variant(request.param)
+    yield request.param
+    cuda_lib.hg_set_gemm_variant(prev)
+
 
 def _run_gemm(hg, a, a_s, w, w_s, off, out=None):
     dev = "cuda"
@@ -54,7 +63,7 @@ def test_config0_full(cuda_lib):
     assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
 
 
-def test_identity_weights(cuda_lib):
+def test_identity_weights(cuda_lib, variant):
     # W = I per expert with unit scales: out = bf16(dequant(A)), exactly
     rng = np.random.default_rng(1)
     E, K = 2, 512
@@ -74,7 +83,7 @@ def test_identity_weights(cuda_lib):
     assert np.array_equal(bf16_bits_to_f64(g), bf16_bits_to_f64(ref))
 
 
-def test_one_hot_weights_distinct_expert_scales(cuda_lib):
+def test_one_hot_weights_distinct_expert_scales(cuda_lib, variant):
     rng = np.random.default_rng(2)
     E, N, K, R = 3, 256, 1024, 300
     a, a_s, _, _ = _rand_codes(rng, R, K, E, N)
@@ -98,7 +107,7 @@ def test_one_hot_weights_distinct_expert_scales(cuda_lib):
     (4, 128, 512, [0, 0, 0, 33, 33]),                     # leading / trailing empty experts
     (2, 512, 3072, [0, 129, 260]),                        # K = 24 stages: the ring wraps many times
 ])
-def test_ragged_experts_random_codes(cuda_lib, E, N, K, cuts):
+def test_ragged_experts_random_codes(cuda_lib, variant, E, N, K, cuts):
     rng = np.random.default_rng(E * 1000 + K)
     R = cuts[-1]
     a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
@@ -107,7 +116,7 @@ def test_ragged_experts_random_codes(cuda_lib, E, N, K, cuts):
     assert_rows_close(bf16_bits(out), ref, f"ragged E={E} N={N} K={K}")
 
 
-def test_wide_scale_range(cuda_lib):
+def test_wide_scale_range(cuda_lib, variant):
     rng = np.random.default_rng(5)
     E, N, K, R = 2, 256, 1024, 70
     a, a_s, w, w_s = _rand_codes(rng, R, K, E, N, scale_lo=107, scale_hi=147)
@@ -117,7 +126,7 @@ def test_wide_scale_range(cuda_lib):
     assert_rows_close(bf16_bits(out), ref, "wide scales")
 
 
-def test_guard_rows_untouched(cuda_lib):
+def test_guard_rows_untouched(cuda_lib, variant):
     # rows at and beyond off[E] belong to no expert and must not be written
     rng = np.random.default_rng(6)
     E, N, K, R = 3, 256, 512, 100
@@ -131,7 +140,7 @@ def test_guard_rows_untouched(cuda_lib):
     assert_rows_close(bf16_bits(out[:61]), ref[:61], "guard")
 
 
-def test_deterministic(cuda_lib):
+def test_deterministic(cuda_lib, variant):
     rng = np.random.default_rng(7)
     E, N, K, R = 4, 512, 2048, 900
     a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
@@ -170,7 +179,7 @@ def test_wait_timeout_is_reported_and_context_survives(cuda_lib):
 
 # ------------------------------------------------ full-size sampled parity --
 
-def _sample_rows(off, rng, per_expert=3, max_experts=6):
+def _sample_rows(off, rng, t_max, per_expert=3, max_experts=6):
     """Expert boundaries, token-tile boundaries and random rows of a few experts."""
     from fp8_mxfp4_grouped_gb300.tiles import token_tiles
     off = np.asarray(off)
@@ -182,13 +191,13 @@ def _sample_rows(off, rng, per_expert=3, max_experts=6):
     for e in sorted(pick):
         lo, hi = int(off[e]), int(off[e + 1])
         rows |= {lo, hi - 1}
-        for r0, valid, _ in token_tiles(hi - lo):
+        for r0, valid, _ in token_tiles(hi - lo, t_max):
             rows |= {lo + r0, lo + r0 + valid - 1}
         rows |= set(int(x) for x in rng.integers(lo, hi, per_expert))
     return np.array(sorted(rows), dtype=np.int64)
 
 
-FULL_CASES = [(1, 64, None, None), (1, 2048, None, None), (2, 64, None, None),
+FULL_CASES = [(1, 64, None, None), (1, 768, None, None), (1, 2048, None, None), (2, 64, None, None),
               (2, 16384, None, None), (3, 1, "w13", None), (3, 256, "w2", None),
               (4, 4096, "gate_up", "uniform"), (4, 4096, "down", "biased")]
 
@@ -203,7 +212,7 @@ def test_full_size_sampled_rows(cuda_lib, cid, M, proj, routing):
     off, *_ = plan_expert_offsets(c.topk_ids, c.E)
     assert np.array_equal(off_t.cpu().numpy(), off)
     rng = np.random.default_rng(cid * 100000 + M)
-    rows = _sample_rows(off, rng)
+    rows = _sample_rows(off, rng, cuda_lib.hg_gemm_token_tile(c.E, c.N, c.K, c.R))
     rr = torch.from_numpy(rows).cuda()
     a = c.a_fp8[rr].cpu().numpy()
     a_s = c.a_scale[rr].cpu().numpy()
