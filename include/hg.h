@@ -98,6 +98,36 @@ hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top
                                  int32_t* src_to_sorted, void* workspace, size_t workspace_bytes,
                                  hg_stream_t stream);
 
+/*
+ * The routing plan without a workspace argument, for callers that cannot
+ * call cudaMalloc where they plan: code that runs while a CUDA graph is being
+ * captured (an allocation is not a stream operation, so it cannot become part
+ * of the graph), hosts that own every device allocation and do not let a
+ * library make its own (framework plugins with a planned memory pool), and
+ * loops that cannot take cudaMalloc's implicit device synchronisation.  The
+ * pages this library follows have no counterpart to this entry point.
+ *
+ * Arguments and results are those of hg_plan_expert_offsets without the
+ * workspace.  The workspace is instead a fixed 256 KiB array in this
+ * library's device memory; every GPU that loads the library holds it until
+ * the process exits.  Shapes whose workspace (hg_plan_workspace_bytes)
+ * exceeds 256 KiB are rejected with HG_ERR_RESOURCE before anything is
+ * launched.  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ * Every call on a device shares the one array, which keeps the last call's
+ * contents; each call overwrites every entry it later reads, so nothing has
+ * to be cleared between calls.  Calls whose executions overlap on the GPU
+ * (different streams, or several host threads) race on the array: put them
+ * on one stream or synchronise between them.  The first call on a device
+ * looks up the array's device address, with that device current; make that
+ * first call before any stream capture.
+ */
+hg_status hg_plan_expert_offsets_noalloc(const int32_t* topk_ids, int32_t M, int32_t top_k,
+                                         int32_t E, int32_t* expert_offsets,
+                                         int32_t* sorted_to_src, int32_t* src_to_sorted,
+                                         hg_stream_t stream);
+
 /* ---------------------------------------------------------------- GEMM -- */
 
 /*
