@@ -49,6 +49,25 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
 
 
+def measured_traffic(M):
+    """ncu DRAM bytes per launch of the GEMM at this M, from the committed profile
+    summary -- only while the kernel source still hashes to the captured version."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", f"grouped_w4a8_gemm_gate_up_M{M}.md")
+    src = os.path.join(ROOT, "fp8_mxfp4_grouped_gb300", "csrc", "gemm.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    fields = {}
+    for line in open(prof):
+        if ":" in line and not line.startswith(("|", "#", " ")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if fields.get("kernel_source_sha256_16") != sha or "dram_bytes_per_launch" not in fields:
+        return None
+    return float(fields["dram_bytes_per_launch"])
+
+
 def algorithmic(R, E_act, E, N, K):
     """GEMM flops and the bytes each operand must cross HBM once."""
     flops = 2.0 * R * N * K
@@ -277,7 +296,7 @@ def run_ours(args, rank, world):
         roof = dict(bound="hbm", achieved=round(dcs["bytes"] / dg / 1e9, 1),
                     peak=peaks["hbm_gbs"], unit="GB/s")
     roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
-    roof["traffic"] = args.traffic
+    roof["traffic"] = measured_traffic(dcs["M"])
     roof["launch"] = f"GEMM at M={dcs['M']} (largest share of the step)"
     roof["peak_source"] = (f"{peaks['source']}: bf16 {peaks['bf16']} TFLOP/s x{FP8_OVER_BF16} "
                            f"nominal fp8/bf16" if roof["bound"] == "tensor"
@@ -424,8 +443,6 @@ def main(argv=None):
     ap.add_argument("--Ms", type=lambda s: [int(x) for x in s.split(",")], default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch of the dominant GEMM launch, if measured")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
