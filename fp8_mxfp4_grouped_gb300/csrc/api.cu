@@ -33,9 +33,12 @@ std::mutex g_dev_mu;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_forced_variant{0};
 
-int choose_variant(int32_t E, int32_t rows) {
-    const int f = g_forced_variant.load();
-    return f ? f : gemm_pick_variant(E, rows);
+int choose_variant(int32_t E, int32_t N, int32_t rows) {
+    int v = g_forced_variant.load();
+    if (!v) v = gemm_pick_variant(E, N, rows);
+    if (v == 4 && N % 256 != 0) v = 3;   // CTA pairs split 256 weight rows
+    if (v == 5 && N % 256 != 0) v = 2;
+    return v;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -185,7 +188,7 @@ hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
     DeviceInfo* d = nullptr;
     hg_status st = device_info(&d);
     if (st != HG_OK) return st;
-    const int variant = choose_variant(E, rows);
+    const int variant = choose_variant(E, N, rows);
     if (static_cast<int>(gemm_smem_bytes(variant, E)) > d->smem_optin) return HG_ERR_RESOURCE;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     st = encoder(&encode);
@@ -269,11 +272,11 @@ hg_status hg_selftest_wait_timeout(uint32_t timeout_us, hg_stream_t stream) {
 
 int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows) {
     if (E < 1 || N < 1 || K < 1 || rows < 0) return 0;
-    return gemm_variant_token_tile(choose_variant(E, rows));
+    return gemm_variant_token_tile(choose_variant(E, N, rows));
 }
 
 int32_t hg_set_gemm_variant(int32_t variant) {
-    if (variant < 0 || variant > 3) return -1;
+    if (variant < 0 || variant > 5) return -1;
     return g_forced_variant.exchange(variant);
 }
 

@@ -85,6 +85,48 @@ struct GemmCfg {
     static_assert(C * 32 * (6 + S) * 96 <= 65536, "registers for C resident CTAs");
 };
 
+// CTA-pair shape (tcgen05 cta_group::2).  T: largest token tile (MMA N,
+// multiple of 32, split in halves between the two CTAs); S: ring stages.
+// Each CTA holds its 128 weight rows and half of the token tile per stage, so
+// a pair computes a 256 x T tile with one MMA instruction stream.
+template <int T, int S, int C>
+struct PairCfg {
+    static constexpr int kTMax = T;
+    static constexpr int kHalf = T / 2;
+    static constexpr int kStages = S;
+    static constexpr int kCtasPerSm = C;
+    static constexpr int kSfWarps = S;
+    static constexpr int kThreads = 32 * (6 + S);
+    static constexpr uint32_t kATileBytes = kHalf * kBK;
+    static constexpr int kSfbAtoms = T > 128 ? 2 : 1;
+    static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
+    static constexpr uint32_t kAccCols = T;
+    static constexpr uint32_t kTmemCols = 512 / C;
+    static constexpr uint32_t kSfCol0 = 2 * kAccCols;
+    static constexpr uint32_t kSfSlotCols = 4 + 4 * kSfbAtoms;
+    static constexpr uint32_t kOffW = 0;
+    static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
+    static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
+    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;
+    static constexpr uint32_t kOffBar = kOffSfb + S * kSfbBytes;
+    static constexpr uint32_t kOffMisc = kOffBar + 256;
+    static constexpr uint32_t kOffSched = kOffMisc + 64;
+    static constexpr size_t smem_bytes(int E) {
+        return kOffSched + static_cast<size_t>(5 * E + 1) * sizeof(int32_t) + 1024;
+    }
+    static constexpr size_t kSmemBudget =
+        C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
+    static_assert(T % 32 == 0 && T >= 32 && T <= 256, "MMA N, split in two halves of 16k");
+    static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
+    static_assert(kSfCol0 + S * kSfSlotCols <= kTmemCols, "TMEM budget");
+    static_assert(smem_bytes(kMaxE) <= kSmemBudget, "shared memory budget");
+    static_assert(8 * (4 * S + 5) <= 256, "barrier area");
+    static_assert(C * 32 * (6 + S) * 96 <= 65536, "registers for C resident CTAs");
+};
+
+using CfgPair = PairCfg<224, 5, 1>;     // many rows per expert, N % 256 == 0
+using CfgPairMid = PairCfg<96, 4, 2>;   // CTA pairs, two pipelines per SM
+
 using CfgSmall = GemmCfg<64, 4, 2>;    // few rows per expert: HBM-bound weight streaming
 using CfgMid = GemmCfg<112, 3, 2>;     // a few hundred rows per expert
 using CfgLarge = GemmCfg<224, 4, 1>;   // many rows per expert: tensor-bound
@@ -433,6 +475,349 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     }
 }
 
+// The same unit walk as grouped_w4a8_kernel, for a CTA pair: unit = (expert,
+// 256 weight rows, token tile).  CTA r of the pair loads weight rows
+// [n0 + 128r, +128) and token rows [row0 + r*half, +half); the even CTA's MMA
+// thread issues M = 256 MMAs that read both CTAs' shared memory and write
+// each CTA's TMEM.  In the odd CTA, the scale warp that owns a ring slot
+// tells the even CTA (remote mbarrier arrive) when that stage is loaded; the
+// even CTA's commits are multicast to both CTAs' barriers.
+template <class Cfg>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
+grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
+                         const __grid_constant__ CUtensorMap map_a,
+                         const __grid_constant__ CUtensorMap map_a64,
+                         const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
+                         const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
+                         uint16_t* __restrict__ out, uint32_t* status, uint64_t timeout_ns) {
+    constexpr int kStages = Cfg::kStages;
+    constexpr int kTMax = Cfg::kTMax;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (sbase - raw_u32);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
+
+    const uint32_t bar_full_tma = sbase + Cfg::kOffBar;
+    const uint32_t bar_full_sf = bar_full_tma + 8 * kStages;
+    const uint32_t bar_peer = bar_full_sf + 8 * kStages;     // leader: the odd CTA's stage is loaded
+    const uint32_t bar_empty = bar_peer + 8 * kStages;
+    const uint32_t bar_tfull = bar_empty + 8 * kStages;
+    const uint32_t bar_tempty = bar_tfull + 16;               // leader: both CTAs drained TMEM
+    const uint32_t bar_done = bar_tempty + 16;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(base + Cfg::kOffMisc);
+    int32_t* s_start = reinterpret_cast<int32_t*>(base + Cfg::kOffSched);
+    int32_t* s_rows = s_start + E;
+    int32_t* s_ntt = s_rows + E;
+    int32_t* s_tile = s_ntt + E;
+    int32_t* s_prefix = s_tile + E;   // E + 1 entries
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar_full_tma + 8 * s, 1);
+            ptx::mbar_init(bar_full_sf + 8 * s, 1);
+            ptx::mbar_init(bar_peer + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_tfull + 8 * b, 1);
+            ptx::mbar_init(bar_tempty + 8 * b, 2 * kEpiWarps);
+        }
+        ptx::mbar_init(bar_done, 1);
+        misc[1] = 0u;   // abort flag
+        ptx::fence_barrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(sbase + Cfg::kOffMisc, Cfg::kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&map_w);
+        ptx::prefetch_tensormap(&map_a);
+        ptx::prefetch_tensormap(&map_a64);
+    }
+
+    // Per-expert token tiling (tiles rounded to 32 rows: two halves of 16k).
+    const int NT = N / (2 * kBW);
+    for (int e = threadIdx.x; e < E; e += Cfg::kThreads) {
+        const int lo = offsets[e];
+        const int hi = offsets[e + 1];
+        int r = 0;
+        if (lo < 0 || hi < lo || hi > rows) {
+            record_error(status, HG_ERR_BAD_OFFSETS, static_cast<uint32_t>(e));
+        } else {
+            r = hi - lo;
+        }
+        const int ntt = (r + kTMax - 1) / kTMax;
+        const int tile = ntt ? ((((r + ntt - 1) / ntt) + 31) & ~31) : 0;
+        s_start[e] = lo;
+        s_rows[e] = r;
+        s_ntt[e] = ntt;
+        s_tile[e] = tile;
+        s_prefix[e] = ntt * NT;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int c = 0; c < E; c += 32) {
+            const int e = c + lane;
+            const int v = e < E ? s_prefix[e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (e < E) s_prefix[e] = carry + incl - v;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) s_prefix[E] = carry;
+    }
+    // Barriers and TMEM of both CTAs must exist before either uses the other's.
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+
+    const uint32_t tmem_base = misc[0];
+    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT};
+    const int U = s_prefix[E];
+    const int KT = K / kBK;
+    const WaitCtx wctx{status, misc + 1, timeout_ns};
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    // Unit geometry for this CTA of the pair.
+    auto unit_of = [&](int u, int& e, int& wrow0, int& row0, int& nrows, int& n_mma) {
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_prefix[mid] <= u) lo = mid; else hi = mid;
+        }
+        e = lo;
+        const int local = u - s_prefix[lo];
+        const int ntt = s_ntt[lo];
+        const int nt = local / ntt;
+        const int tt = local - nt * ntt;
+        const int tile = s_tile[lo];
+        wrow0 = nt * 2 * kBW;                      // first weight row of the pair's 256
+        row0 = s_start[lo] + tt * tile;
+        nrows = min(tile, s_rows[lo] - tt * tile);
+        n_mma = (nrows + 31) & ~31;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_a = ptx::policy_evict_last();
+            uint32_t g = 0;
+            bool ok = true;
+            for (int u = pair; ok && u < U; u += npairs) {
+                int e, wrow0, row0, nrows, n_mma;
+                unit_of(u, e, wrow0, row0, nrows, n_mma);
+                const int half = n_mma / 2;
+                const int wrow = e * N + wrow0 + static_cast<int>(rank) * kBW;
+                const int arow = row0 + static_cast<int>(rank) * half;
+                const int nbig = half / kABigRows;
+                const int nsmall = (half - nbig * kABigRows) / kABoxRows;
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const uint32_t slot = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1u;
+                    if (!wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleProducer, slot)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full_tma + 8 * slot;
+                    ptx::mbar_arrive_expect_tx(fb, kWTileTx + half * kBK);
+                    ptx::tma_load_2d(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w, ks * kBK,
+                                     wrow, fb, pol_w);
+                    const uint32_t adst = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
+                    for (int j = 0; j < nbig; ++j) {
+                        ptx::tma_load_2d(adst + j * kABigBytes, &map_a64, ks * kBK,
+                                         arow + j * kABigRows, fb, pol_a);
+                    }
+                    const int r0 = nbig * kABigRows;
+                    for (int j = 0; j < nsmall; ++j) {
+                        ptx::tma_load_2d(adst + (r0 + j * kABoxRows) * kBK, &map_a, ks * kBK,
+                                         arow + r0 + j * kABoxRows, fb, pol_a);
+                    }
+                }
+            }
+            const uint32_t first = g > kStages ? g - kStages : 0;
+            for (uint32_t gg = first; gg < g; ++gg) {
+                wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            // --------------------------------------- MMA issuer (pair) ---
+            uint32_t g = 0, tc = 0;
+            bool ok = true;
+            for (int u = pair; ok && u < U; u += npairs, ++tc) {
+                int e, wrow0, row0, nrows, n_mma;
+                unit_of(u, e, wrow0, row0, nrows, n_mma);
+                const uint32_t b = tc & 1u;
+                if (!wait_bounded<true>(bar_tempty + 8 * b, ((tc >> 1) & 1u) ^ 1u, wctx, kRoleMma,
+                                        0x100u | b)) {
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t idesc0 =
+                    ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, 2 * kBW, n_mma);
+                const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
+                for (int ks = 0; ks < KT; ++ks, ++g) {
+                    const uint32_t slot = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1u;
+                    if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
+                        !wait_bounded(bar_full_sf + 8 * slot, ph, wctx, kRoleMma, 0x10u | slot) ||
+                        !wait_bounded<true>(bar_peer + 8 * slot, ph, wctx, kRoleMma, 0x20u | slot)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
+                    const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
+                    const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
+                    ptx::tc_cp_32x128b_warpx4_pair(sf_col, ptx::desc_sf_32x16(sfa));
+                    ptx::tc_cp_32x128b_warpx4_pair(sf_col + 4, ptx::desc_sf_32x16(sfb));
+                    if (Cfg::kSfbAtoms > 1 && n_mma > 128) {
+                        ptx::tc_cp_32x128b_warpx4_pair(sf_col + 8, ptx::desc_sf_32x16(sfb + 512));
+                    }
+                    const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
+                    const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk) {
+                        ptx::mma_mxf8f6f4_1x_pair(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
+                                                  ptx::desc_kmajor_sw128(asm_ + kk * 32),
+                                                  ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
+                                                  sf_col + 4, (ks | kk) != 0 ? 1u : 0u);
+                    }
+                    ptx::tc_commit_pair_multicast(bar_empty + 8 * slot, 0x3);
+                }
+                if (!ok) break;
+                ptx::tc_commit_pair_multicast(bar_tfull + 8 * b, 0x3);
+            }
+            // Everything issued must finish before either CTA releases TMEM.
+            ptx::tc_commit_pair_multicast(bar_done, 0x1);
+            wait_drain(bar_done, 0u, timeout_ns);
+        }
+    } else if (warp >= 4 && warp < 4 + kEpiWarps) {
+        // ---------------------------------------------------- epilogue --
+        const int q = warp & 3;
+        const uint32_t tempty_leader = ptx::mapa_shared(bar_tempty, 0);
+        uint32_t tc = 0;
+        for (int u = pair; u < U; u += npairs, ++tc) {
+            int e, wrow0, row0, nrows, n_mma;
+            unit_of(u, e, wrow0, row0, nrows, n_mma);
+            const uint32_t b = tc & 1u;
+            if (!wait_bounded<true>(bar_tfull + 8 * b, (tc >> 1) & 1u, wctx, kRoleEpilogue, b)) break;
+            ptx::tc_fence_after();
+            const int n = wrow0 + static_cast<int>(rank) * kBW + 32 * q + lane;
+            uint16_t* dst = out + static_cast<size_t>(row0) * N + n;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
+            for (int c0 = 0; c0 < nrows; c0 += 16) {
+                uint32_t v[16];
+                ptx::tmem_ld_32x32b_x16(taddr + c0, v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (c0 + j < nrows) {
+                        dst[static_cast<size_t>(c0 + j) * N] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_remote(tempty_leader + 8 * b);
+        }
+    } else {
+        // ------------------------------------------- scale staging -----
+        // Weight scales of this CTA's 128 rows; token scales of the WHOLE
+        // token tile (each CTA's TMEM needs all N columns' scales).
+        const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;
+        const int ws_row = K / 32;
+        const int as_row = K / kBK;
+        const uint32_t peer_bar0 = ptx::mapa_shared(bar_peer, 0);
+        uint32_t g = 0;
+        bool ok = true;
+        for (int u = pair; ok && u < U; u += npairs) {
+            int e, wrow0, row0, nrows, n_mma;
+            unit_of(u, e, wrow0, row0, nrows, n_mma);
+            const uint8_t* wsrc =
+                w_scale + static_cast<size_t>(e * N + wrow0 + static_cast<int>(rank) * kBW + lane) *
+                              ws_row;
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                if (static_cast<int>(g % Cfg::kSfWarps) != sfw) continue;
+                const uint32_t slot = g % kStages;
+                const uint32_t ph = (g / kStages) & 1u;
+                uint32_t wv[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    wv[c] = ldg_u32(wsrc + static_cast<size_t>(32 * c) * ws_row + ks * 4);
+                }
+                uint32_t av[4 * Cfg::kSfbAtoms];
+#pragma unroll
+                for (int i = 0; i < 4 * Cfg::kSfbAtoms; ++i) {
+                    const int tok = 128 * (i >> 2) + lane + 32 * (i & 3);
+                    const int r = row0 + tok;
+                    av[i] = 0x7F7F7F7Fu;
+                    if (tok < n_mma && r < rows) {
+                        av[i] = static_cast<uint32_t>(
+                                    __ldg(a_scale + static_cast<size_t>(r) * as_row + ks)) *
+                                0x01010101u;
+                    }
+                }
+                if (!wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleScale, slot)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes + 16 * lane;
+                const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes + 16 * lane;
+                sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
+                sts_v4(sfb, av[0], av[1], av[2], av[3]);
+                if (Cfg::kSfbAtoms > 1 && n_mma > 128) {
+                    sts_v4(sfb + 512, av[4 % (4 * Cfg::kSfbAtoms)], av[5 % (4 * Cfg::kSfbAtoms)],
+                           av[6 % (4 * Cfg::kSfbAtoms)], av[7 % (4 * Cfg::kSfbAtoms)]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader) {
+                        ptx::mbar_arrive(bar_full_sf + 8 * slot);
+                    } else {
+                        // The odd CTA's stage is complete once its own TMA
+                        // bytes have landed; publish both to the even CTA.
+                        if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleRelay, slot)) {
+                            ok = false;
+                        } else {
+                            ptx::mbar_arrive_remote(peer_bar0 + 8 * slot);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+            }
+        }
+    }
+
+    // Neither CTA may release TMEM or shared memory while the pair's MMAs or
+    // the other CTA's remote arrivals can still touch them.
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    }
+}
+
 __global__ void selftest_wait_kernel(uint32_t* status, uint64_t timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t abort_flag;
@@ -476,6 +861,30 @@ cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtens
     return cudaGetLastError();
 }
 
+template <class Cfg>
+cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
+                        const CUtensorMap& map_a64, cudaStream_t stream) {
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t err = cudaFuncSetAttribute(grouped_w4a8_pair_kernel<Cfg>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(Cfg::smem_bytes(kMaxE)));
+        if (err != cudaSuccess) return err;
+        configured = true;
+    }
+    const long long nt = a.N / (2 * kBW);
+    const long long active = a.E < a.rows ? a.E : a.rows;
+    const long long units_max = ((a.rows + Cfg::kTMax - 1) / Cfg::kTMax + active) * nt;
+    long long pairs = static_cast<long long>(a.num_sms / 2) * Cfg::kCtasPerSm;
+    if (units_max < pairs) pairs = units_max;
+    if (pairs < 1) return cudaSuccess;
+    grouped_w4a8_pair_kernel<Cfg><<<static_cast<int>(2 * pairs), Cfg::kThreads,
+                                    Cfg::smem_bytes(a.E), stream>>>(
+        map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.out,
+        a.status, a.timeout_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 int gemm_max_experts() { return kMaxE; }
@@ -483,7 +892,8 @@ int gemm_max_experts() { return kMaxE; }
 // Variant choice from the mean rows per expert (the per-expert counts live on
 // the device).  Few rows: weight streaming dominates and two small pipelines
 // per SM keep the MMA issue rate up; many rows: the widest token tile.
-int gemm_pick_variant(int32_t E, int32_t rows) {
+int gemm_pick_variant(int32_t E, int32_t N, int32_t rows) {
+    (void)N;
     const long long per = rows / (E > 0 ? E : 1);
     if (per <= 48) return 1;
     if (per <= 640) return 2;
@@ -495,6 +905,8 @@ int gemm_variant_token_tile(int variant) {
         case 1: return CfgSmall::kTMax;
         case 2: return CfgMid::kTMax;
         case 3: return CfgLarge::kTMax;
+        case 4: return CfgPair::kTMax;
+        case 5: return CfgPairMid::kTMax;
         default: return 0;
     }
 }
@@ -503,6 +915,8 @@ size_t gemm_smem_bytes(int variant, int32_t E) {
     switch (variant) {
         case 1: return CfgSmall::smem_bytes(E);
         case 2: return CfgMid::smem_bytes(E);
+        case 4: return CfgPair::smem_bytes(E);
+        case 5: return CfgPairMid::smem_bytes(E);
         default: return CfgLarge::smem_bytes(E);
     }
 }
@@ -513,6 +927,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
     switch (a.variant) {
         case 1: return launch_cfg<CfgSmall>(a, map_w, map_a, map_a64, stream);
         case 2: return launch_cfg<CfgMid>(a, map_w, map_a, map_a64, stream);
+        case 4: return launch_pair<CfgPair>(a, map_w, map_a, map_a64, stream);
+        case 5: return launch_pair<CfgPairMid>(a, map_w, map_a, map_a64, stream);
         default: return launch_cfg<CfgLarge>(a, map_w, map_a, map_a64, stream);
     }
 }

@@ -33,6 +33,7 @@ enum WaitRole : uint32_t {
     kRoleEpilogue = 4,
     kRoleTeardown = 5,
     kRoleSelftest = 6,
+    kRoleRelay = 7,
 };
 
 struct WaitCtx {
@@ -44,13 +45,20 @@ struct WaitCtx {
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up
 // after ctx.timeout_ns (records HG_ERR_TIMEOUT and raises the CTA's abort
 // flag) or as soon as another role of the CTA raised the abort flag.
-// Returns true when the phase completed.
+// Returns true when the phase completed.  kCluster: acquire at cluster scope
+// (for barriers that threads of another CTA of the cluster arrive on).
+template <bool kCluster = false>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+    return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+}
+
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                              uint32_t role, uint32_t where) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_wait_scoped<kCluster>(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (try_wait_scoped<kCluster>(bar, parity)) return true;
         if (*ctx.abort) return false;
         if ((it & 7u) == 0u && ptx::globaltimer_ns() - t0 > ctx.timeout_ns) {
             *ctx.abort = 1u;
@@ -73,7 +81,7 @@ struct GemmArgs {
     uint32_t* status;
     uint64_t timeout_ns;
     int num_sms;
-    int variant;   // 1 small tiles / 2 CTAs per SM, 2 mid, 3 large tiles / 1 CTA per SM
+    int variant;   // 1 small tiles / 2 CTAs per SM, 2 mid, 3 large tiles / 1 CTA per SM, 4 CTA pairs
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
@@ -81,7 +89,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
                                 cudaStream_t stream);
 size_t gemm_smem_bytes(int variant, int32_t E);
 int gemm_max_experts();
-int gemm_pick_variant(int32_t E, int32_t rows);
+int gemm_pick_variant(int32_t E, int32_t N, int32_t rows);
 int gemm_variant_token_tile(int variant);
 
 struct PlanArgs {

@@ -20,12 +20,13 @@ T_MAX depends on the pipeline variant the library picks from rows / E
 from __future__ import annotations
 
 T_MAX = 224
-VARIANT_T_MAX = {1: 64, 2: 112, 3: 224}
+VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96}
+VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32}   # CTA pairs split the token tile in two
 MMA_N_STEP = 16
 W_TILE = 128
 
 
-def pick_variant(E: int, rows: int) -> int:
+def pick_variant(E: int, N: int, rows: int) -> int:
     """Mirror of the library's variant choice (mean rows per expert)."""
     per = rows // max(E, 1)
     if per <= 48:
@@ -35,24 +36,24 @@ def pick_variant(E: int, rows: int) -> int:
     return 3
 
 
-def expert_tiling(rows_e: int, t_max: int = T_MAX):
+def expert_tiling(rows_e: int, t_max: int = T_MAX, step: int = MMA_N_STEP):
     """(n_t, tile) for one expert; (0, 0) for an empty expert."""
     if rows_e <= 0:
         return 0, 0
     n_t = -(-rows_e // t_max)
     per = -(-rows_e // n_t)
-    tile = -(-per // MMA_N_STEP) * MMA_N_STEP
+    tile = -(-per // step) * step
     return n_t, tile
 
 
-def token_tiles(rows_e: int, t_max: int = T_MAX):
+def token_tiles(rows_e: int, t_max: int = T_MAX, step: int = MMA_N_STEP):
     """List of (first_row, valid_rows, mma_n) of one expert's token tiles."""
-    n_t, tile = expert_tiling(rows_e, t_max)
+    n_t, tile = expert_tiling(rows_e, t_max, step)
     out = []
     for tt in range(n_t):
         r0 = tt * tile
         valid = min(tile, rows_e - r0)
-        out.append((r0, valid, -(-valid // MMA_N_STEP) * MMA_N_STEP))
+        out.append((r0, valid, -(-valid // step) * step))
     return out
 
 

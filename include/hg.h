@@ -176,8 +176,12 @@ int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows);
  * Force the GEMM pipeline variant for later calls in this process: 0 = choose
  * automatically (default), 1 = 64-row token tiles with two CTAs per SM,
  * 2 = 112-row tiles with two CTAs per SM, 3 = 224-row tiles with one CTA per
- * SM.  Meant for tests and tuning.  Returns the previous setting, or -1 for
- * an invalid value (setting unchanged).  Host-only.
+ * SM, 4 = 224-row tiles on CTA pairs (256 weight rows per pair; used only
+ * when N % 256 == 0, else variant 3), 5 = 96-row tiles on CTA pairs with two
+ * pairs per SM pair (N % 256 == 0, else variant 2).  Meant for tests and
+ * tuning.  Returns
+ * the previous setting, or -1 for an invalid value (setting unchanged).
+ * Host-only.
  */
 int32_t hg_set_gemm_variant(int32_t variant);
 

@@ -17,7 +17,7 @@ from tests.gpu_util import assert_rows_close, bf16_bits, np_u8
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [1, 2, 3]   # 64-row / 112-row tiles with 2 CTAs per SM, 224-row tiles with 1
+VARIANTS = [1, 2, 3, 4, 5]   # see hg_set_gemm_variant
 
 
 @pytest.fixture(params=VARIANTS, ids=lambda v: f"variant{v}")
@@ -213,6 +213,7 @@ def test_full_size_sampled_rows(cuda_lib, cid, M, proj, routing):
     assert np.array_equal(off_t.cpu().numpy(), off)
     rng = np.random.default_rng(cid * 100000 + M)
     rows = _sample_rows(off, rng, cuda_lib.hg_gemm_token_tile(c.E, c.N, c.K, c.R))
+    # (token-tile boundaries are sampled with 16-row rounding; pairs round to 32 rows)
     rr = torch.from_numpy(rows).cuda()
     a = c.a_fp8[rr].cpu().numpy()
     a_s = c.a_scale[rr].cpu().numpy()

@@ -9,39 +9,46 @@ from oracle.plan import plan_expert_offsets
 from synth import make_routing
 
 
-@pytest.mark.parametrize("t_max", [64, 112, 224])
+@pytest.mark.parametrize("t_max,step", [(64, 16), (112, 16), (224, 16), (224, 32)])
 @pytest.mark.parametrize("rows", list(range(0, 700)) + [1000, 4096, 14618])
-def test_tiles_cover_rows_once(rows, t_max):
-    ts = T.token_tiles(rows, t_max)
+def test_tiles_cover_rows_once(rows, t_max, step):
+    ts = T.token_tiles(rows, t_max, step)
     covered = []
     for r0, valid, mma_n in ts:
         assert 0 < valid <= t_max
-        assert mma_n % 16 == 0 and valid <= mma_n <= t_max and mma_n - valid < 16
+        assert mma_n % step == 0 and valid <= mma_n <= t_max and mma_n - valid < step
         covered.extend(range(r0, r0 + valid))
     assert covered == list(range(rows))
     # fewest tiles: any tiling with tiles of at most t_max rows needs ceil(rows / t_max)
     assert len(ts) == -(-rows // t_max)
 
 
-@pytest.mark.parametrize("t_max", [64, 112, 224])
-def test_brute_force_minimal_tile_size(t_max):
-    # for each row count, the chosen tile is the smallest multiple of 16 that
-    # covers the rows with the minimal number of tiles
+@pytest.mark.parametrize("t_max,step", [(64, 16), (112, 16), (224, 16), (224, 32)])
+def test_brute_force_minimal_tile_size(t_max, step):
+    # for each row count, the chosen tile is the smallest multiple of the MMA
+    # step that covers the rows with the minimal number of tiles
     for rows in range(1, 1200):
-        n_t, tile = T.expert_tiling(rows, t_max)
-        best = min(t for t in range(16, t_max + 1, 16) if -(-rows // t) == n_t)
+        n_t, tile = T.expert_tiling(rows, t_max, step)
+        best = min(t for t in range(step, t_max + 1, step) if -(-rows // t) == n_t)
         assert tile == best, rows
 
 
 def test_variant_choice_mirrors_the_library():
     from fp8_mxfp4_grouped_gb300 import hg
     for E in (1, 4, 12, 32, 100, 512):
-        for rows in (0, 1, 16, 48 * E, 48 * E + E, 640 * E, 640 * E + E, 131072):
-            v = T.pick_variant(E, rows)
-            assert hg.hg_gemm_token_tile(E, 4096, 6144, rows) == T.VARIANT_T_MAX[v], (E, rows)
+        for N in (256, 3584, 4096, 6144):
+            for rows in (0, 1, 16, 48 * E, 48 * E + E, 640 * E, 640 * E + E, 131072):
+                v = T.pick_variant(E, N, rows)
+                assert hg.hg_gemm_token_tile(E, N, 6144, rows) == T.VARIANT_T_MAX[v], (E, N, rows)
     prev = hg.hg_set_gemm_variant(2)
     try:
         assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 112
+        hg.hg_set_gemm_variant(4)
+        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 224
+        assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 224   # falls back to variant 3
+        hg.hg_set_gemm_variant(5)
+        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 96
+        assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 112   # falls back to variant 2
     finally:
         hg.hg_set_gemm_variant(prev)
     with pytest.raises(ValueError):
