@@ -172,10 +172,14 @@ hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top
     return launch_plan(a, s) == cudaSuccess ? HG_OK : HG_ERR_CUDA;
 }
 
-hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
-                               const uint8_t* w_fp4, const uint8_t* w_scale,
-                               const int32_t* expert_offsets, int32_t E, int32_t N, int32_t K,
-                               int32_t rows, uint16_t* out_bf16, hg_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scale_mmajor,
+                       const uint8_t* w_fp4, const uint8_t* w_scale,
+                       const int32_t* expert_offsets, int32_t E, int32_t N, int32_t K,
+                       int32_t rows, uint16_t* out_bf16, hg_stream_t stream) {
     if (E < 1 || N < 1 || K < 1 || rows < 0) return HG_ERR_INVALID_ARG;
     if (!w_fp4 || !w_scale || !expert_offsets) return HG_ERR_INVALID_ARG;
     if (rows > 0 && (!a_fp8 || !a_scale || !out_bf16)) return HG_ERR_INVALID_ARG;
@@ -232,6 +236,8 @@ hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
     a.N = N;
     a.K = K;
     a.rows = rows;
+    a.as_rs = a_scale_mmajor ? 1 : K / 128;
+    a.as_ks = a_scale_mmajor ? rows : 1;
     a.out = out_bf16;
     a.status = d->status;
     a.timeout_ns = g_timeout_ns.load();
@@ -239,6 +245,66 @@ hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
     a.variant = variant;
     return launch_grouped_gemm(a, map_w, map_a, map_a64, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
+               ? HG_OK
+               : HG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
+                               const uint8_t* w_fp4, const uint8_t* w_scale,
+                               const int32_t* expert_offsets, int32_t E, int32_t N, int32_t K,
+                               int32_t rows, uint16_t* out_bf16, hg_stream_t stream) {
+    return grouped_gemm(a_fp8, a_scale, false, w_fp4, w_scale, expert_offsets, E, N, K, rows,
+                        out_bf16, stream);
+}
+
+hg_status hg_grouped_w4a8_gemm_mmajor(const uint8_t* a_fp8, const uint8_t* a_scale_mmajor,
+                                      const uint8_t* w_fp4, const uint8_t* w_scale,
+                                      const int32_t* expert_offsets, int32_t E, int32_t N,
+                                      int32_t K, int32_t rows, uint16_t* out_bf16,
+                                      hg_stream_t stream) {
+    return grouped_gemm(a_fp8, a_scale_mmajor, true, w_fp4, w_scale, expert_offsets, E, N, K,
+                        rows, out_bf16, stream);
+}
+
+hg_status hg_quantize_gather_acts(const uint16_t* x_bf16, int32_t M, int32_t K, int32_t top_k,
+                                  const int32_t* sorted_to_src, uint8_t* a_fp8,
+                                  uint8_t* a_scale, hg_stream_t stream) {
+    if (M < 0 || K < 1 || top_k < 1) return HG_ERR_INVALID_ARG;
+    if (K % 128 != 0) return HG_ERR_UNSUPPORTED_SHAPE;
+    const long long rows = static_cast<long long>(M) * top_k;
+    if (rows > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return HG_OK;
+    if (!x_bf16 || !sorted_to_src || !a_fp8 || !a_scale) return HG_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(a_fp8, 16)) return HG_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    hg_status st = device_info(&d);
+    if (st != HG_OK) return st;
+    return launch_quantize_gather(x_bf16, K, top_k, sorted_to_src, static_cast<int>(rows), a_fp8,
+                                  a_scale, d->num_sms,
+                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HG_OK
+               : HG_ERR_CUDA;
+}
+
+hg_status hg_combine_topk(const uint16_t* y_bf16, const int32_t* src_to_sorted,
+                          const float* topk_weights, int32_t M, int32_t top_k, int32_t N,
+                          uint16_t* out_bf16, hg_stream_t stream) {
+    if (M < 0 || top_k < 1 || N < 1) return HG_ERR_INVALID_ARG;
+    if (N % 8 != 0) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<long long>(M) * top_k > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return HG_OK;
+    if (!y_bf16 || !src_to_sorted || !topk_weights || !out_bf16) return HG_ERR_INVALID_ARG;
+    if (!aligned(y_bf16, 16) || !aligned(out_bf16, 16) || !aligned(topk_weights, 4))
+        return HG_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    hg_status st = device_info(&d);
+    if (st != HG_OK) return st;
+    return launch_combine_topk(y_bf16, src_to_sorted, topk_weights, M, top_k, N, out_bf16,
+                               d->num_sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HG_OK
                : HG_ERR_CUDA;
 }

@@ -197,7 +197,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     const __grid_constant__ CUtensorMap map_a64,
                     const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
                     const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
-                    uint16_t* __restrict__ out, uint32_t* status, uint64_t timeout_ns) {
+                    int as_rs, int as_ks, uint16_t* __restrict__ out, uint32_t* status,
+                    uint64_t timeout_ns) {
     constexpr int kStages = Cfg::kStages;
     constexpr int kTMax = Cfg::kTMax;
     extern __shared__ uint8_t smem_raw[];
@@ -417,7 +418,6 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         // ------------------------------------------- scale staging -----
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;   // warps 2, 3, 8, 9, ...
         const int ws_row = K / 32;     // bytes per w_scale row
-        const int as_row = K / kBK;    // bytes per a_scale row
         uint32_t g = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
@@ -444,7 +444,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     av[i] = 0x7F7F7F7Fu;
                     if (tok < t.n_mma && r < rows) {
                         av[i] = static_cast<uint32_t>(
-                                    __ldg(a_scale + static_cast<size_t>(r) * as_row + ks)) *
+                                    __ldg(a_scale + static_cast<size_t>(r) * as_rs +
+                                          static_cast<size_t>(ks) * as_ks)) *
                                 0x01010101u;
                     }
                 }
@@ -489,7 +490,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                          const __grid_constant__ CUtensorMap map_a64,
                          const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
                          const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
-                         uint16_t* __restrict__ out, uint32_t* status, uint64_t timeout_ns) {
+                         int as_rs, int as_ks, uint16_t* __restrict__ out, uint32_t* status,
+                         uint64_t timeout_ns) {
     constexpr int kStages = Cfg::kStages;
     constexpr int kTMax = Cfg::kTMax;
     extern __shared__ uint8_t smem_raw[];
@@ -743,7 +745,6 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         // token tile (each CTA's TMEM needs all N columns' scales).
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;
         const int ws_row = K / 32;
-        const int as_row = K / kBK;
         const uint32_t peer_bar0 = ptx::mapa_shared(bar_peer, 0);
         uint32_t g = 0;
         bool ok = true;
@@ -770,7 +771,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                     av[i] = 0x7F7F7F7Fu;
                     if (tok < n_mma && r < rows) {
                         av[i] = static_cast<uint32_t>(
-                                    __ldg(a_scale + static_cast<size_t>(r) * as_row + ks)) *
+                                    __ldg(a_scale + static_cast<size_t>(r) * as_rs +
+                                          static_cast<size_t>(ks) * as_ks)) *
                                 0x01010101u;
                     }
                 }
@@ -857,7 +859,8 @@ cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtens
     if (grid < 1) return cudaSuccess;
     grouped_w4a8_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
                                stream>>>(map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets,
-                                         a.E, a.N, a.K, a.rows, a.out, a.status, a.timeout_ns);
+                                         a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out, a.status,
+                                         a.timeout_ns);
     return cudaGetLastError();
 }
 
@@ -880,8 +883,8 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const CUten
     if (pairs < 1) return cudaSuccess;
     grouped_w4a8_pair_kernel<Cfg><<<static_cast<int>(2 * pairs), Cfg::kThreads,
                                     Cfg::smem_bytes(a.E), stream>>>(
-        map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.out,
-        a.status, a.timeout_ns);
+        map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs,
+        a.as_ks, a.out, a.status, a.timeout_ns);
     return cudaGetLastError();
 }
 

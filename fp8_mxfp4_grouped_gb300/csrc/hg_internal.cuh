@@ -77,6 +77,7 @@ struct GemmArgs {
     const uint8_t* w_scale;
     const int32_t* offsets;
     int32_t E, N, K, rows;
+    int32_t as_rs, as_ks;   // a_scale element (row r, group g) is at r * as_rs + g * as_ks
     uint16_t* out;
     uint32_t* status;
     uint64_t timeout_ns;
@@ -111,5 +112,12 @@ size_t plan_smem_bytes(int32_t E, int threads);
 bool plan_small_fits(int32_t R, int32_t E, int smem_limit);
 
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+cudaError_t launch_quantize_gather(const uint16_t* x, int K, int top_k, const int32_t* s2d,
+                                   int rows, uint8_t* a_fp8, uint8_t* a_scale, int num_sms,
+                                   cudaStream_t stream);
+cudaError_t launch_combine_topk(const uint16_t* y, const int32_t* d2s, const float* weights,
+                                int M, int top_k, int N, uint16_t* out, int num_sms,
+                                cudaStream_t stream);
 
 }  // namespace hg

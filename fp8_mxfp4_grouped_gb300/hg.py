@@ -39,6 +39,12 @@ lib.hg_plan_expert_offsets.argtypes = [_p, _i32, _i32, _i32, _p, _p, _p, _p, _sz
 lib.hg_plan_expert_offsets.restype = ctypes.c_int
 lib.hg_grouped_w4a8_gemm.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _p]
 lib.hg_grouped_w4a8_gemm.restype = ctypes.c_int
+lib.hg_grouped_w4a8_gemm_mmajor.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _p]
+lib.hg_grouped_w4a8_gemm_mmajor.restype = ctypes.c_int
+lib.hg_quantize_gather_acts.argtypes = [_p, _i32, _i32, _i32, _p, _p, _p, _p]
+lib.hg_quantize_gather_acts.restype = ctypes.c_int
+lib.hg_combine_topk.argtypes = [_p, _p, _p, _i32, _i32, _i32, _p, _p]
+lib.hg_combine_topk.restype = ctypes.c_int
 lib.hg_get_device_status.argtypes = [_p, ctypes.POINTER(_u32)]
 lib.hg_get_device_status.restype = ctypes.c_int
 lib.hg_selftest_wait_timeout.argtypes = [_u32, _p]
@@ -130,6 +136,56 @@ def hg_grouped_w4a8_gemm(a_fp8: torch.Tensor, a_scale: torch.Tensor, w_fp4: torc
                                   _ptr(expert_offsets), E, N, K, rows, _ptr(out),
                                   _stream(stream))
     _check(st, "hg_grouped_w4a8_gemm")
+    return out
+
+
+def hg_grouped_w4a8_gemm_mmajor(a_fp8: torch.Tensor, a_scale_mmajor: torch.Tensor,
+                                w_fp4: torch.Tensor, w_scale: torch.Tensor,
+                                expert_offsets: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """The GEMM with activation scales laid out [K/128, rows]. Returns out [rows, N] bf16."""
+    E, N, K2 = w_fp4.shape
+    K = 2 * K2
+    rows = a_fp8.shape[0]
+    for t in (a_fp8, a_scale_mmajor, w_fp4, w_scale, expert_offsets):
+        assert t.is_contiguous()
+    assert a_fp8.shape == (rows, K) and a_scale_mmajor.shape == (K // 128, rows)
+    assert w_scale.shape == (E, N, K // 32) and expert_offsets.numel() == E + 1
+    if out is None:
+        out = torch.empty((rows, N), dtype=torch.bfloat16, device=a_fp8.device)
+    st = lib.hg_grouped_w4a8_gemm_mmajor(_ptr(a_fp8), _ptr(a_scale_mmajor), _ptr(w_fp4),
+                                         _ptr(w_scale), _ptr(expert_offsets), E, N, K, rows,
+                                         _ptr(out), _stream(stream))
+    _check(st, "hg_grouped_w4a8_gemm_mmajor")
+    return out
+
+
+def hg_quantize_gather_acts(x_bf16: torch.Tensor, top_k: int, sorted_to_src: torch.Tensor,
+                            a_fp8=None, a_scale=None, stream=None):
+    """BF16 [M, K] tokens -> (E4M3 [M*top_k, K], E8M0 [M*top_k, K/128]) in sorted order."""
+    assert x_bf16.dtype == torch.bfloat16 and x_bf16.is_contiguous() and x_bf16.dim() == 2
+    M, K = x_bf16.shape
+    R = M * top_k
+    if a_fp8 is None:
+        a_fp8 = torch.empty((R, K), dtype=torch.uint8, device=x_bf16.device)
+    if a_scale is None:
+        a_scale = torch.empty((R, K // 128), dtype=torch.uint8, device=x_bf16.device)
+    st = lib.hg_quantize_gather_acts(_ptr(x_bf16), M, K, top_k, _ptr(sorted_to_src), _ptr(a_fp8),
+                                     _ptr(a_scale), _stream(stream))
+    _check(st, "hg_quantize_gather_acts")
+    return a_fp8, a_scale
+
+
+def hg_combine_topk(y_bf16: torch.Tensor, src_to_sorted: torch.Tensor, topk_weights: torch.Tensor,
+                    out=None, stream=None) -> torch.Tensor:
+    """out[t] = sum_j w[t, j] * y[src_to_sorted[t*k + j]]  (FP32 sum, BF16 result)."""
+    M, k = topk_weights.shape
+    N = y_bf16.shape[1]
+    assert topk_weights.dtype == torch.float32 and topk_weights.is_contiguous()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=y_bf16.device)
+    st = lib.hg_combine_topk(_ptr(y_bf16), _ptr(src_to_sorted), _ptr(topk_weights), M, k, N,
+                             _ptr(out), _stream(stream))
+    _check(st, "hg_combine_topk")
     return out
 
 

@@ -166,6 +166,18 @@ hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
                                int32_t rows, uint16_t* out_bf16, hg_stream_t stream);
 
 /*
+ * The same GEMM with the activation scales in M-major order [H129 benchmark
+ * command, option --use_m_major_input_scale]: a_scale_mmajor is uint8
+ * [K/128, rows], the scale of row r for 128-K group g at g * rows + r.  All
+ * other arguments, results and errors as hg_grouped_w4a8_gemm.
+ */
+hg_status hg_grouped_w4a8_gemm_mmajor(const uint8_t* a_fp8, const uint8_t* a_scale_mmajor,
+                                      const uint8_t* w_fp4, const uint8_t* w_scale,
+                                      const int32_t* expert_offsets, int32_t E, int32_t N,
+                                      int32_t K, int32_t rows, uint16_t* out_bf16,
+                                      hg_stream_t stream);
+
+/*
  * Largest token tile (MMA N) hg_grouped_w4a8_gemm uses for these arguments:
  * an expert with r rows is cut into ceil(r / T) tiles of equal size rounded
  * up to 16 rows.  Host-only query; 0 for invalid arguments.
@@ -184,6 +196,45 @@ int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows);
  * Host-only.
  */
 int32_t hg_set_gemm_variant(int32_t variant);
+
+/* ------------------------------------------------ around the GEMM (MoE) -- */
+
+/*
+ * Quantise BF16 token activations to the GEMM's input format and gather them
+ * into the plan's sorted order in one pass.  Row r of the output takes token
+ * t = sorted_to_src[r] / top_k; rows with sorted_to_src[r] < 0 are not
+ * written.  Per 128-element group of a row: e = the smallest integer with
+ * amax <= 448 * 2^e (amax = 0 gives e = 0), clamped to [-127, 127];
+ * a_scale = 127 + e (E8M0); a_fp8 = E4M3 round-to-nearest-even of x / 2^e.
+ * A group holding an Inf or NaN gets scale code 0xFF and element codes 0x7F
+ * (the NaN codes of both formats).  The cast is the 128-group counterpart of
+ * the rowwise MXFP8 cast of TransformerEngine PR #3459 ("non-TMA MXFP8
+ * cast-only kernels", description).
+ *
+ *   x_bf16         uint16 [M, K] BF16 bit patterns, 16-byte aligned.
+ *   sorted_to_src  int32 [M*top_k] from hg_plan_expert_offsets.
+ *   a_fp8          uint8 [M*top_k, K] out, 16-byte aligned; a_scale uint8 [M*top_k, K/128] out.
+ * K % 128 == 0.  One kernel on `stream`; no host synchronisation.
+ */
+hg_status hg_quantize_gather_acts(const uint16_t* x_bf16, int32_t M, int32_t K, int32_t top_k,
+                                  const int32_t* sorted_to_src, uint8_t* a_fp8,
+                                  uint8_t* a_scale, hg_stream_t stream);
+
+/*
+ * Combine the experts' outputs back into token order with the router's top-k
+ * weights: out[t, :] = bf16_rne( sum_j w[t, j] * y[src_to_sorted[t*top_k + j], :] ),
+ * the sum in FP32 over j ascending; terms with src_to_sorted < 0 (ids the
+ * plan dropped) are skipped.
+ *
+ *   y_bf16         uint16 [M*top_k, N] BF16 (the GEMM output), 16-byte aligned.
+ *   src_to_sorted  int32 [M*top_k] from hg_plan_expert_offsets.
+ *   topk_weights   float32 [M, top_k].
+ *   out_bf16       uint16 [M, N] out, 16-byte aligned.
+ * N % 8 == 0.  One kernel on `stream`; no host synchronisation.
+ */
+hg_status hg_combine_topk(const uint16_t* y_bf16, const int32_t* src_to_sorted,
+                          const float* topk_weights, int32_t M, int32_t top_k, int32_t N,
+                          uint16_t* out_bf16, hg_stream_t stream);
 
 /* ------------------------------------------------------------- status -- */
 

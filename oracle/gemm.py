@@ -117,3 +117,15 @@ def rows_outputs(a_fp8, a_scale, w_fp4, w_scale, expert_offsets, rows_idx):
         w_hat = dequant_weights(np.asarray(w_fp4)[ee], np.asarray(w_scale)[ee])
         vals[sel] = a_hat @ w_hat.T
     return round_f64_to_bf16_bits(vals)
+
+
+def grouped_w4a8_gemm_mmajor(a_fp8, a_scale_mmajor, w_fp4, w_scale, expert_offsets, E, N, K):
+    """BF16 bits of the GEMM with the activation scales stored M-major.
+
+    humming PR #129 benchmark command, option ``--use_m_major_input_scale``:
+    the activation scales are laid out ``[K/128, rows]`` (the scale of row r
+    for 128-K group g at ``[g, r]``) instead of ``[rows, K/128]``; the method
+    is otherwise unchanged.
+    """
+    a_scale_rows = np.ascontiguousarray(np.asarray(a_scale_mmajor, dtype=np.uint8).T)
+    return grouped_w4a8_gemm(a_fp8, a_scale_rows, w_fp4, w_scale, expert_offsets, E, N, K)

@@ -275,3 +275,33 @@ def test_graph_capture_replay_matches_eager(cuda_lib):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(bf16_bits(out), eager)
+
+
+# ----------------------------------------------------- M-major activation scales --
+
+@pytest.mark.parametrize("E,N,K,cuts", [(6, 384, 1024, [0, 1, 17, 17, 240, 470, 700]),
+                                        (2, 512, 3072, [0, 129, 260])])
+def test_mmajor_scales_ragged(cuda_lib, variant, E, N, K, cuts):
+    rng = np.random.default_rng(E * 77 + K)
+    R = cuts[-1]
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    a_mm = np.ascontiguousarray(a_s.T)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    out = cuda_lib.hg_grouped_w4a8_gemm_mmajor(t(a), t(a_mm), t(w), t(w_s),
+                                               t(np.asarray(cuts, dtype=np.int32)))
+    torch.cuda.synchronize()
+    ref = G.grouped_w4a8_gemm_mmajor(a, a_mm, w, w_s, cuts, E, N, K)
+    assert_rows_close(bf16_bits(out), ref, f"m-major E={E} N={N} K={K}")
+
+
+@pytest.mark.parametrize("cid,M", [(1, 512), (2, 64)])
+def test_mmajor_matches_row_major_full_size(cuda_lib, cid, M):
+    # same codes, scales transposed: the two entry points must agree bit for bit
+    c = make_case(cid, M, device="cuda")
+    off, _, _ = cuda_lib.hg_plan_expert_offsets(torch.from_numpy(c.topk_ids).cuda(), c.E)
+    o_row = cuda_lib.hg_grouped_w4a8_gemm(c.a_fp8, c.a_scale, c.w_fp4, c.w_scale, off)
+    o_mm = cuda_lib.hg_grouped_w4a8_gemm_mmajor(c.a_fp8, c.a_scale.t().contiguous(), c.w_fp4,
+                                                c.w_scale, off)
+    torch.cuda.synchronize()
+    assert torch.equal(o_row.view(torch.int16), o_mm.view(torch.int16))
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK

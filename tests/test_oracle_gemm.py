@@ -216,3 +216,26 @@ def test_rows_outputs_equal_full_outputs():
     full = G.grouped_w4a8_gemm(a, s, w, ws, off, E, N, K)
     idx = np.array([29, 0, 8, 9, 19, 20, 26, 27, 3])
     assert np.array_equal(G.rows_outputs(a, s, w, ws, off, idx), full[idx])
+
+
+def test_mmajor_scales_index_groups_by_row():
+    # M-major scales: element [g, r]; check against a direct per-element sum
+    # written with that indexing (not through the row-major path)
+    rng = np.random.default_rng(16)
+    E, N, K, R = 2, 128, 256, 6
+    a, s_rows = _rand_acts(rng, R, K)
+    s_mm = np.ascontiguousarray(s_rows.T)               # [K/128, R]
+    w = _pack(rng.integers(0, 16, (E, N, K), dtype=np.uint8))
+    ws = rng.integers(124, 131, (E, N, K // 32), dtype=np.uint8)
+    off = np.array([0, 4, 6], dtype=np.int32)
+    got = G.grouped_w4a8_gemm_mmajor(a, s_mm, w, ws, off, E, N, K)
+    for r in range(R):
+        e = 0 if r < 4 else 1
+        for n in range(0, N, 13):
+            acc = Fraction(0)
+            for k in range(K):
+                byte = int(w[e, n, k // 2])
+                nib = (byte & 0xF) if k % 2 == 0 else (byte >> 4)
+                acc += (_bf_e4m3(int(a[r, k])) * Fraction(2) ** (int(s_mm[k // 128, r]) - 127)
+                        * _bf_e2m1(nib) * Fraction(2) ** (int(ws[e, n, k // 32]) - 127))
+            assert int(got[r, n]) == _bf_bf16_rne(acc), (r, n)
