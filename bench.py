@@ -342,6 +342,8 @@ def run_ours(args, rank, world):
         e2e = dict(value=round(flops_e2e / tot / 1e12, 2), unit=UNIT, h2d_bytes_per_step=int(bi),
                    d2h_bytes_per_step=int(bo))
 
+    moe_io = None if args.no_moe_io else time_moe_io(cases[-1], flush, stream, peaks, hg)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(Ms[0])
@@ -358,6 +360,7 @@ def run_ours(args, rank, world):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "sweep": sweep,
         "roofline": roof,
+        "moe_io": moe_io,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 3 * len(cases) * args.steps,
@@ -365,6 +368,48 @@ def run_ours(args, rank, world):
         "wall_s_timed": round(t_wall, 3),
     }
     return line
+
+
+def time_moe_io(cs, flush, stream, peaks, hg, reps=20):
+    """Device time of the kernels around the GEMM at the sweep's largest M:
+    BF16 -> E4M3 quantise + gather into sorted order, and the top-k combine.
+    Both are HBM-bound; roofline = algorithmic bytes / HBM peak."""
+    c, b = cs["c"], cs["bufs"]
+    M, K, N, k, R = c.M, c.K, c.N, c.top_k, cs["R"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(77)
+    x = torch.randn((M, K), generator=gen, device="cuda").to(torch.bfloat16)
+    w = torch.rand((M, k), generator=gen, device="cuda")
+    a = torch.empty((R, K), dtype=torch.uint8, device="cuda")
+    s = torch.empty((R, K // 128), dtype=torch.uint8, device="cuda")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    hg.hg_plan_expert_offsets(b["ids"], c.E, b["off"], b["s2d"], b["d2s"], b["ws"], stream=stream)
+
+    def timed(fn):
+        ts = []
+        for it in range(reps + 3):
+            with torch.cuda.stream(stream):
+                flush.fill_(it & 0xFF)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            if it >= 3:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(x0.elapsed_time(x1) for x0, x1 in ts) * 1e3
+
+    tq = timed(lambda: hg.hg_quantize_gather_acts(x, k, b["s2d"], a, s, stream=stream))
+    tc = timed(lambda: hg.hg_combine_topk(b["out"], b["d2s"], w, out, stream=stream))
+    bq = M * K * 2 + R * 4 + R * K + R * K / 128
+    bc = R * N * 2 + R * 4 + M * k * 4 + M * N * 2
+    hbm = peaks["hbm_gbs"]
+    return {"M": M, "quantize_gather_us": round(tq, 2), "quantize_gather_gbs": round(bq / tq / 1e3, 1),
+            "quantize_gather_roof_frac": round(bq / tq / 1e3 / hbm, 3),
+            "combine_us": round(tc, 2), "combine_gbs": round(bc / tc / 1e3, 1),
+            "combine_roof_frac": round(bc / tc / 1e3 / hbm, 3),
+            "bytes": {"quantize_gather": int(bq), "combine": int(bc)}}
 
 
 # ------------------------------------------------------------ oracle arms --
@@ -443,6 +488,7 @@ def main(argv=None):
     ap.add_argument("--Ms", type=lambda s: [int(x) for x in s.split(",")], default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-moe-io", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

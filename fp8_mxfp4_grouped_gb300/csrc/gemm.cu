@@ -78,10 +78,16 @@ struct GemmCfg {
     }
     static constexpr size_t kSmemBudget =
         C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
+    // experts whose scheduler tables still fit next to the ring (<= kMaxE)
+    static constexpr int kMaxExperts =
+        (static_cast<long long>(kSmemBudget) - static_cast<long long>(smem_bytes(0))) / 20 < kMaxE
+            ? static_cast<int>((kSmemBudget - smem_bytes(0)) / 20)
+            : kMaxE;
     static_assert(T % 16 == 0 && T >= 16 && T <= 256, "MMA N");
     static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
     static_assert(kSfCol0 + S * kSfSlotCols <= kTmemCols, "TMEM budget");
-    static_assert(smem_bytes(kMaxE) <= kSmemBudget, "shared memory budget");
+    static_assert(kMaxExperts >= 32 && smem_bytes(kMaxExperts) <= kSmemBudget,
+                  "shared memory budget");
     static_assert(C * 32 * (6 + S) * 96 <= 65536, "registers for C resident CTAs");
 };
 
@@ -845,7 +851,7 @@ cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtens
     if (!configured) {
         cudaError_t err = cudaFuncSetAttribute(grouped_w4a8_kernel<Cfg>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(Cfg::smem_bytes(kMaxE)));
+                                               static_cast<int>(Cfg::smem_bytes(Cfg::kMaxExperts)));
         if (err != cudaSuccess) return err;
         configured = true;
     }
@@ -891,6 +897,15 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const CUten
 }  // namespace
 
 int gemm_max_experts() { return kMaxE; }
+
+int gemm_variant_max_experts(int variant) {
+    switch (variant) {
+        case 1: return CfgSmall::kMaxExperts;
+        case 2: return CfgMid::kMaxExperts;
+        case 3: return CfgLarge::kMaxExperts;
+        default: return kMaxE;
+    }
+}
 
 // Variant choice from the mean rows per expert (the per-expert counts live on
 // the device).  Few rows: weight streaming dominates and two small pipelines

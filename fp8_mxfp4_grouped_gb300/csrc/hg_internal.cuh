@@ -92,6 +92,7 @@ size_t gemm_smem_bytes(int variant, int32_t E);
 int gemm_max_experts();
 int gemm_pick_variant(int32_t E, int32_t N, int32_t rows);
 int gemm_variant_token_tile(int variant);
+int gemm_variant_max_experts(int variant);
 
 struct PlanArgs {
     const int32_t* ids;
