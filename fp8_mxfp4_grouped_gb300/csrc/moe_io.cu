@@ -44,79 +44,96 @@ __device__ __forceinline__ int scale_exponent(float amax) {
     return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// One half-warp per 128-element group: lane j of the half holds elements
-// 8j .. 8j+7 (one 16-byte load, one 8-byte store).
-__global__ void quantize_gather_kernel(const uint16_t* __restrict__ x, int K, int top_k,
-                                       const int32_t* __restrict__ sorted_to_src, int rows,
-                                       uint8_t* __restrict__ a_fp8, uint8_t* __restrict__ a_scale) {
-    const int groups_per_row = K / kGroup;
-    const long long total = static_cast<long long>(rows) * groups_per_row;
-    const int half = (threadIdx.x >> 4) & 1;
-    const int j = threadIdx.x & 15;
-    const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 4);
-    for (long long gi = static_cast<long long>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
-         gi - half < total; gi += stride) {
-        // both halves of a warp iterate together; a half past the end idles
-        const bool active = gi < total;
-        long long r = 0;
-        int g = 0, src = -1;
-        if (active) {
-            r = gi / groups_per_row;
-            g = static_cast<int>(gi - r * groups_per_row);
-            src = __ldg(sorted_to_src + r);
-        }
-        const bool live = active && src >= 0;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (live) {
-            const long long t = src / top_k;
-            v = __ldg(reinterpret_cast<const uint4*>(x + t * K + g * kGroup) + j);
-        }
-        float f[8];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// One 256-thread block per sorted row and iteration: the row's source index is
+// read once, then each half-warp takes groups hw, hw+16, hw+32, ... of the row
+// with all its 16-byte loads issued before any is used (lane j of the half
+// holds elements 8j .. 8j+7 of a group).
+constexpr int kQThreads = 256;
+constexpr int kQHalves = kQThreads / 16;
+constexpr int kQMaxIter = 4;                       // groups per half-warp held in registers
+
+__device__ __forceinline__ void quantize_group(const uint4 v, uint8_t* dst, uint8_t* scale_dst,
+                                               int j) {
+    float f[8];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-        float amax = 0.0f;
-        bool nonfinite = false;
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float amax = 0.0f;
+    bool nonfinite = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        amax = fmaxf(amax, fabsf(f[i]));
+        nonfinite |= !isfinite(f[i]);
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite ? 1 : 0, o) != 0;
+    }
+    if (dst == nullptr) return;
+    uint8_t code_scale;
+    uint32_t lo, hi;
+    if (nonfinite) {
+        code_scale = 0xFF;                         // E8M0 NaN
+        lo = hi = 0x7F7F7F7Fu;                     // E4M3 NaN
+    } else {
+        const int e = scale_exponent(amax);
+        code_scale = static_cast<uint8_t>(127 + e);
+        // 2^-e from its bits: finite BF16 inputs give e <= 120, so the
+        // biased exponent 127 - e stays in [7, 254] (a normal float).
+        const float inv = __int_as_float((127 - e) << 23);
+        uint32_t b[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            amax = fmaxf(amax, fabsf(f[i]));
-            nonfinite |= !isfinite(f[i]);
+            b[i] = __nv_cvt_float_to_fp8(f[i] * inv, __NV_SATFINITE, __NV_E4M3);
         }
+        lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+        hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+    }
+    *reinterpret_cast<uint2*>(dst + 8 * j) = make_uint2(lo, hi);
+    if (j == 0) *scale_dst = code_scale;
+}
+
+__global__ void __launch_bounds__(kQThreads)
+quantize_gather_kernel(const uint16_t* __restrict__ x, int K, int top_k,
+                       const int32_t* __restrict__ sorted_to_src, int rows,
+                       uint8_t* __restrict__ a_fp8, uint8_t* __restrict__ a_scale) {
+    const int G = K / kGroup;
+    const int hw = threadIdx.x >> 4;
+    const int j = threadIdx.x & 15;
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int src = __ldg(sorted_to_src + r);
+        if (src < 0) continue;                              // uniform across the block
+        const uint16_t* xrow = x + static_cast<long long>(src / top_k) * K;
+        uint8_t* arow = a_fp8 + static_cast<long long>(r) * K;
+        uint8_t* srow = a_scale + static_cast<long long>(r) * G;
+        for (int g0 = 0; g0 < G; g0 += kQHalves * kQMaxIter) {
+            uint4 v[kQMaxIter];
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) {
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite ? 1 : 0, o) != 0;
-        }
-        if (!live) continue;
-        uint8_t code_scale;
-        uint32_t lo = 0, hi = 0;
-        if (nonfinite) {
-            code_scale = 0xFF;                       // E8M0 NaN
-            lo = hi = 0x7F7F7F7Fu;                   // E4M3 NaN
-        } else {
-            const int e = scale_exponent(amax);
-            code_scale = static_cast<uint8_t>(127 + e);
-            // 2^-e from its bits: finite BF16 inputs give e <= 120, so the
-            // biased exponent 127 - e stays in [7, 254] (a normal float).
-            const float inv = __int_as_float((127 - e) << 23);
-            uint32_t b[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                b[i] = __nv_cvt_float_to_fp8(f[i] * inv, __NV_SATFINITE, __NV_E4M3);
+            for (int k = 0; k < kQMaxIter; ++k) {
+                const int g = g0 + hw + kQHalves * k;
+                v[k] = make_uint4(0, 0, 0, 0);
+                if (g < G) v[k] = __ldg(reinterpret_cast<const uint4*>(xrow + g * kGroup) + j);
             }
-            lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-            hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+#pragma unroll
+            for (int k = 0; k < kQMaxIter; ++k) {
+                const int g = g0 + hw + kQHalves * k;
+                // every lane takes part in the half-warp reductions; only
+                // lanes of a real group write
+                quantize_group(v[k], g < G ? arow + g * kGroup : nullptr, srow + g, j);
+            }
         }
-        uint8_t* dst = a_fp8 + r * K + g * kGroup + 8 * j;
-        *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-        if (j == 0) a_scale[r * groups_per_row + g] = code_scale;
     }
 }
 
-// One warp per token, 8 output columns (16 bytes) per lane per step.
+// One warp per token: lanes 0..top_k-1 fetch the token's sorted rows and
+// weights, the warp shares them by shuffles, then every lane loads its 16
+// bytes of each of the top_k rows before accumulating (8 at a time).
+constexpr int kCBatch = 8;
+
 __global__ void combine_topk_kernel(const uint16_t* __restrict__ y,
                                     const int32_t* __restrict__ src_to_sorted,
                                     const float* __restrict__ weights, int M, int top_k, int N,
@@ -128,16 +145,40 @@ __global__ void combine_topk_kernel(const uint16_t* __restrict__ y,
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            for (int jj = 0; jj < top_k; ++jj) {
-                const int r = __ldg(src_to_sorted + static_cast<long long>(t) * top_k + jj);
-                if (r < 0) continue;
-                const float wgt = __ldg(weights + static_cast<long long>(t) * top_k + jj);
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<long long>(r) * N + n0));
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            for (int j0 = 0; j0 < top_k; j0 += 32) {
+                int my_r = -1;
+                float my_w = 0.0f;
+                if (j0 + lane < top_k) {
+                    my_r = __ldg(src_to_sorted + static_cast<long long>(t) * top_k + j0 + lane);
+                    my_w = __ldg(weights + static_cast<long long>(t) * top_k + j0 + lane);
+                }
+                const int nj = min(32, top_k - j0);
+                for (int b0 = 0; b0 < nj; b0 += kCBatch) {
+                    uint4 v[kCBatch];
+                    float wj[kCBatch];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = fmaf(wgt, __uint_as_float(w4[i] << 16), acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(wgt, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                    for (int jj = 0; jj < kCBatch; ++jj) {
+                        const int r = __shfl_sync(0xFFFFFFFFu, my_r, (b0 + jj) & 31);
+                        wj[jj] = __shfl_sync(0xFFFFFFFFu, my_w, (b0 + jj) & 31);
+                        v[jj] = make_uint4(0, 0, 0, 0);
+                        if (b0 + jj < nj && r >= 0) {
+                            v[jj] = __ldg(reinterpret_cast<const uint4*>(
+                                y + static_cast<long long>(r) * N + n0));
+                        } else {
+                            wj[jj] = 0.0f;
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < kCBatch; ++jj) {
+                        if (b0 + jj >= nj) break;
+                        const uint32_t w4[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc[2 * i] = fmaf(wj[jj], __uint_as_float(w4[i] << 16), acc[2 * i]);
+                            acc[2 * i + 1] =
+                                fmaf(wj[jj], __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                        }
+                    }
                 }
             }
             uint32_t o[4];
@@ -158,13 +199,12 @@ __global__ void combine_topk_kernel(const uint16_t* __restrict__ y,
 cudaError_t launch_quantize_gather(const uint16_t* x, int K, int top_k, const int32_t* s2d,
                                    int rows, uint8_t* a_fp8, uint8_t* a_scale, int num_sms,
                                    cudaStream_t stream) {
-    const long long groups = static_cast<long long>(rows) * (K / kGroup);
-    long long blocks = (groups + 15) / 16;           // 256 threads = 16 groups per pass
+    long long blocks = rows;                         // one sorted row per block and pass
     const long long cap = static_cast<long long>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
-    quantize_gather_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(x, K, top_k, s2d, rows,
-                                                                       a_fp8, a_scale);
+    quantize_gather_kernel<<<static_cast<int>(blocks), kQThreads, 0, stream>>>(
+        x, K, top_k, s2d, rows, a_fp8, a_scale);
     return cudaGetLastError();
 }
 
