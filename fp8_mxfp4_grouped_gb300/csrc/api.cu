@@ -33,9 +33,9 @@ std::mutex g_dev_mu;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_forced_variant{0};
 
-int choose_variant(int32_t E, int32_t N, int32_t rows) {
+int choose_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms) {
     int v = g_forced_variant.load();
-    if (!v) v = gemm_pick_variant(E, N, rows);
+    if (!v) v = gemm_pick_variant(E, N, K, rows, num_sms);
     if (v == 4 && N % 256 != 0) v = 3;   // CTA pairs split 256 weight rows
     if (v == 5 && N % 256 != 0) v = 2;
     return v;
@@ -192,7 +192,7 @@ hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scal
     DeviceInfo* d = nullptr;
     hg_status st = device_info(&d);
     if (st != HG_OK) return st;
-    const int variant = choose_variant(E, N, rows);
+    const int variant = choose_variant(E, N, K, rows, d->num_sms);
     if (static_cast<int>(gemm_smem_bytes(variant, E)) > d->smem_optin) return HG_ERR_RESOURCE;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     st = encoder(&encode);
@@ -338,11 +338,29 @@ hg_status hg_selftest_wait_timeout(uint32_t timeout_us, hg_stream_t stream) {
 
 int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows) {
     if (E < 1 || N < 1 || K < 1 || rows < 0) return 0;
-    return gemm_variant_token_tile(choose_variant(E, N, rows));
+    DeviceInfo* d = nullptr;
+    const int sms = device_info(&d) == HG_OK ? d->num_sms : 0;
+    return gemm_variant_token_tile(choose_variant(E, N, K, rows, sms));
+}
+
+int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows) {
+    if (E < 1 || E > gemm_max_experts() || N < 128 || N % 128 != 0 || K < 512 || K % 512 != 0 ||
+        rows < 0)
+        return 0;
+    DeviceInfo* d = nullptr;
+    if (device_info(&d) != HG_OK) return -1;
+    GemmArgs a{};
+    a.E = E;
+    a.N = N;
+    a.K = K;
+    a.rows = rows;
+    a.num_sms = d->num_sms;
+    a.variant = choose_variant(E, N, K, rows, d->num_sms);
+    return static_cast<int32_t>(gemm_launch_ctas(a));
 }
 
 int32_t hg_set_gemm_variant(int32_t variant) {
-    if (variant < 0 || variant > 5) return -1;
+    if (variant < 0 || variant > 6) return -1;
     return g_forced_variant.exchange(variant);
 }
 

@@ -26,6 +26,8 @@
 //  * every barrier wait is bounded (see wait_bounded).
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "hg_internal.cuh"
 
 namespace hg {
@@ -41,7 +43,6 @@ constexpr uint32_t kWTileBytes = kBW * kBK;    // unpacked E2M1: one byte of sme
 // The 16U4_ALIGN16B TMA load writes 8 data bytes into each 16-byte chunk and
 // leaves the other 8 untouched; its transaction count is the packed bytes.
 constexpr uint32_t kWTileTx = kBW * kBK / 2;
-constexpr uint32_t kABoxBytes = kABoxRows * kBK;
 constexpr uint32_t kABigBytes = kABigRows * kBK;
 constexpr uint32_t kSfaBytes = 512;            // 128 rows x 4 blocks of 32 K
 constexpr uint32_t kSmemPerSm = 233472;        // 228 KB per SM on sm_103
@@ -52,11 +53,21 @@ constexpr uint32_t kSmemReservedPerBlock = 1024;
 // resident per SM.  Each CTA is a complete pipeline; with C = 2 two MMA
 // issuers share the SM's tensor core (one thread issues one MMA per ~80-130
 // cycles, so small tiles need two issuers to keep up with HBM).
-template <int T, int S, int C>
+// CL > 1: the grid runs as clusters of CL CTAs, and the kernel may split the
+// K loop of every unit over 2 or CL of them (split-K, chosen on the device
+// from the unit count); each CTA then holds receive slots for the FP32
+// partial tiles of the others.
+template <int T, int S, int C, int CL = 1>
 struct GemmCfg {
     static constexpr int kTMax = T;
     static constexpr int kStages = S;
     static constexpr int kCtasPerSm = C;
+    static constexpr int kCluster = CL;
+    // A CTA of a split group finalises 4/s of the four TMEM lane quadrants
+    // and receives s-1 partials of each: (4/s)(s-1) slots, at most 3.
+    static constexpr uint32_t kRxSlotBytes = 32 * T * 4;     // one lane quadrant, FP32
+    static constexpr int kRxSlots = CL == 1 ? 0 : (CL == 2 ? 2 : 3);
+    static constexpr uint32_t kRxBytes = kRxSlots * kRxSlotBytes;
     static constexpr int kSfWarps = S;                     // one scale warp per ring slot
     static constexpr int kThreads = 32 * (6 + S);          // TMA, MMA, 4 epilogue, S scale warps
     static constexpr uint32_t kATileBytes = T * kBK;
@@ -70,7 +81,8 @@ struct GemmCfg {
     static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
     static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
     static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;
-    static constexpr uint32_t kOffBar = kOffSfb + S * kSfbBytes;
+    static constexpr uint32_t kOffRx = kOffSfb + S * kSfbBytes;
+    static constexpr uint32_t kOffBar = kOffRx + kRxBytes;
     static constexpr uint32_t kOffMisc = kOffBar + 256;
     static constexpr uint32_t kOffSched = kOffMisc + 64;
     static constexpr size_t smem_bytes(int E) {
@@ -78,6 +90,8 @@ struct GemmCfg {
     }
     static constexpr size_t kSmemBudget =
         C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
+    static_assert(CL == 1 || CL == 2 || CL == 4, "split over 2 or 4 CTAs");
+    static_assert(8 * (3 * S + 5 + 8) <= 256, "barrier area");
     // experts whose scheduler tables still fit next to the ring (<= kMaxE)
     static constexpr int kMaxExperts =
         (static_cast<long long>(kSmemBudget) - static_cast<long long>(smem_bytes(0))) / 20 < kMaxE
@@ -136,6 +150,24 @@ using CfgPairMid = PairCfg<96, 4, 2>;   // CTA pairs, two pipelines per SM
 using CfgSmall = GemmCfg<64, 4, 2>;    // few rows per expert: HBM-bound weight streaming
 using CfgMid = GemmCfg<112, 3, 2>;     // a few hundred rows per expert
 using CfgLarge = GemmCfg<224, 4, 1>;   // many rows per expert: tensor-bound
+using CfgSplit = GemmCfg<32, 4, 2, 4>; // few units per CTA: split-K over clusters of 4
+
+// Split-K factor for a launch of G CTAs (a multiple of max_split) over U
+// units of KT stages: the s in {1, 2, 4} that minimises the stages of the
+// busiest CTA, ceil(U / (G / s)) * KT / s; ties keep the smaller split.
+__host__ __device__ __forceinline__ int choose_split(int U, int KT, int G, int max_split) {
+    int best = 1;
+    long long best_cost = static_cast<long long>((U + G - 1) / G) * KT;
+    for (int s = 2; s <= max_split; s <<= 1) {
+        const int groups = G / s;
+        const long long c = static_cast<long long>((U + groups - 1) / groups) * (KT / s);
+        if (c < best_cost) {
+            best_cost = c;
+            best = s;
+        }
+    }
+    return best;
+}
 
 struct Sched {
     const int32_t* start;
@@ -207,6 +239,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     uint64_t timeout_ns) {
     constexpr int kStages = Cfg::kStages;
     constexpr int kTMax = Cfg::kTMax;
+    constexpr int kCL = Cfg::kCluster;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -221,6 +254,10 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     const uint32_t bar_tfull = bar_empty + 8 * kStages;
     const uint32_t bar_tempty = bar_tfull + 16;
     const uint32_t bar_done = bar_tempty + 16;
+    // split-K: per lane quadrant, "partials received" (arrive + bytes) and
+    // "my partial consumed by its owner" (one remote arrive)
+    const uint32_t bar_rx_full = bar_done + 8;
+    const uint32_t bar_tx_free = bar_rx_full + 32;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(base + Cfg::kOffMisc);
     int32_t* s_start = reinterpret_cast<int32_t*>(base + Cfg::kOffSched);
     int32_t* s_rows = s_start + E;
@@ -239,6 +276,12 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             ptx::mbar_init(bar_tempty + 8 * b, kEpiWarps);
         }
         ptx::mbar_init(bar_done, 1);
+        if (kCL > 1) {
+            for (int q = 0; q < 4; ++q) {
+                ptx::mbar_init(bar_rx_full + 8 * q, 1);
+                ptx::mbar_init(bar_tx_free + 8 * q, 1);
+            }
+        }
         misc[1] = 0u;   // abort flag
         ptx::fence_barrier_init();
     }
@@ -289,7 +332,12 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         if (lane == 0) s_prefix[E] = carry;
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if (kCL > 1) {
+        __syncwarp();
+        ptx::cluster_sync();   // every CTA's barriers exist before any remote arrive
+    } else {
+        __syncthreads();
+    }
     ptx::tc_fence_after();
 
     const uint32_t tmem_base = misc[0];
@@ -297,6 +345,15 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     const int U = s_prefix[E];
     const int KT = K / kBK;
     const WaitCtx wctx{status, misc + 1, timeout_ns};
+    // Split-K: groups of `split` consecutive CTAs (inside one cluster) share
+    // each unit, CTA krank of a group taking stages [k0, k1).  Every CTA
+    // derives the same split from U.
+    const int split = kCL > 1 ? choose_split(U, KT, static_cast<int>(gridDim.x), kCL) : 1;
+    const int krank = kCL > 1 ? static_cast<int>(blockIdx.x) % split : 0;
+    const int gid = static_cast<int>(blockIdx.x) / split;
+    const int ngroups = static_cast<int>(gridDim.x) / split;
+    const int k0 = krank * (KT / split);
+    const int k1 = k0 + KT / split;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
@@ -305,12 +362,12 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             const uint64_t pol_a = ptx::policy_evict_last();
             uint32_t g = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+            for (int u = gid; ok && u < U; u += ngroups) {
                 const Unit t = decode_unit(sch, u);
                 const int wrow = t.e * N + t.n0;
                 const int nbig = t.n_mma / kABigRows;
                 const int nsmall = (t.n_mma - nbig * kABigRows) / kABoxRows;
-                for (int ks = 0; ks < KT; ++ks, ++g) {
+                for (int ks = k0; ks < k1; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
                     if (!wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleProducer, slot)) {
@@ -345,7 +402,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         if (lane == 0) {
             uint32_t g = 0, tc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < U; u += gridDim.x, ++tc) {
+            for (int u = gid; ok && u < U; u += ngroups, ++tc) {
                 const Unit t = decode_unit(sch, u);
                 const uint32_t b = tc & 1u;
                 if (!wait_bounded(bar_tempty + 8 * b, ((tc >> 1) & 1u) ^ 1u, wctx, kRoleMma,
@@ -356,7 +413,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 const uint32_t idesc0 =
                     ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, kBW, t.n_mma);
                 const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
-                for (int ks = 0; ks < KT; ++ks, ++g) {
+                for (int ks = k0; ks < k1; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
                     if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
@@ -380,7 +437,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                         ptx::mma_mxf8f6f4_1x(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
                                              ptx::desc_kmajor_sw128(asm_ + kk * 32),
                                              ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
-                                             sf_col + 4, (ks | kk) != 0 ? 1u : 0u);
+                                             sf_col + 4, (ks != k0 || kk != 0) ? 1u : 0u);
                     }
                     ptx::tc_commit(bar_empty + 8 * slot);
                 }
@@ -394,25 +451,106 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     } else if (warp >= 4 && warp < 4 + kEpiWarps) {
         // ---------------------------------------------------- epilogue --
         const int q = warp & 3;   // TMEM lane quadrant this warp may read
+        // Split-K reduce-scatter: quadrant q of every unit is finalised by
+        // group rank `owner`; the other ranks send it their FP32 partial of
+        // that quadrant (st.async into the owner's receive slot), and the
+        // owner adds the partials in K order (rank 0 first), so the result
+        // does not depend on timing.
+        const int owner = (q * split) >> 2;
+        const bool finalise = owner == krank;
+        const uint32_t rank0 = kCL > 1 ? ptx::cluster_ctarank() - krank : 0;   // group's first CTA
+        const int per_owner = 4 / split;                       // quadrants each rank finalises
+        const uint32_t rx_base =
+            sbase + Cfg::kOffRx + (q - owner * per_owner) * (split - 1) * Cfg::kRxSlotBytes;
         uint32_t tc = 0;
-        for (int u = blockIdx.x; u < U; u += gridDim.x, ++tc) {
+        bool armed = false;   // a receive was announced and not yet seen complete
+        for (int u = gid; u < U; u += ngroups, ++tc) {
             const Unit t = decode_unit(sch, u);
             const uint32_t b = tc & 1u;
             if (!wait_bounded(bar_tfull + 8 * b, (tc >> 1) & 1u, wctx, kRoleEpilogue, b)) break;
             ptx::tc_fence_after();
-            const int n = t.n0 + 32 * q + lane;
-            uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
-            for (int c0 = 0; c0 < t.nrows; c0 += 16) {
-                uint32_t v[16];
-                ptx::tmem_ld_32x32b_x16(taddr + c0, v);
-                ptx::tmem_ld_wait();
+            if (kCL > 1 && !finalise) {
+                // ---- send this quadrant's partial to its owner
+                if (!wait_bounded<true>(bar_tx_free + 8 * q, (tc & 1u) ^ 1u, wctx, kRoleEpilogue,
+                                        0x200u | q)) {
+                    break;
+                }
+                const uint32_t dst_rank = rank0 + owner;
+                const int slot = (krank - owner - 1 + split) % split;
+                const uint32_t dst =
+                    ptx::mapa_shared(rx_base + slot * Cfg::kRxSlotBytes + 16 * lane, dst_rank);
+                const uint32_t dbar = ptx::mapa_shared(bar_rx_full + 8 * q, dst_rank);
+                for (int c0 = 0; c0 < t.n_mma; c0 += 16) {
+                    uint32_t v[16];
+                    ptx::tmem_ld_32x32b_x16(taddr + c0, v);
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (c0 + j < t.nrows) {
-                        dst[static_cast<size_t>(c0 + j) * N] =
-                            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                    for (int jj = 0; jj < 4; ++jj) {
+                        // layout [column / 4][lane][column % 4]
+                        ptx::st_async_v4(dst + (c0 / 4 + jj) * 512, v[4 * jj], v[4 * jj + 1],
+                                         v[4 * jj + 2], v[4 * jj + 3], dbar);
+                    }
+                }
+            } else {
+                // ---- finalise: own partial (+ the others' in K order) -> BF16
+                if (kCL > 1 && split > 1) {
+                    const uint32_t rxb = bar_rx_full + 8 * q;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(
+                            rxb, static_cast<uint32_t>((split - 1) * 32 * t.n_mma * 4));
+                    }
+                    armed = true;
+                    if (!wait_bounded<true>(rxb, tc & 1u, wctx, kRoleEpilogue, 0x300u | q)) break;
+                    armed = false;
+                }
+                const int n = t.n0 + 32 * q + lane;
+                uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
+                const float4* rx = reinterpret_cast<const float4*>(
+                    base + (rx_base - sbase)) + lane;
+                for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+                    uint32_t v[16];
+                    ptx::tmem_ld_32x32b_x16(taddr + c0, v);
+                    ptx::tmem_ld_wait();
+                    float acc[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+                    for (int k = 0; k < split; ++k) {
+                        if (k == krank) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] += __uint_as_float(v[j]);
+                        } else {
+                            const int slot = (k - krank - 1 + split) % split;
+                            const float4* p = rx + slot * (Cfg::kRxSlotBytes / 16) + (c0 / 4) * 32;
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) {
+                                const float4 w = p[jj * 32];
+                                acc[4 * jj] += w.x;
+                                acc[4 * jj + 1] += w.y;
+                                acc[4 * jj + 2] += w.z;
+                                acc[4 * jj + 3] += w.w;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (c0 + j < t.nrows) {
+                            dst[static_cast<size_t>(c0 + j) * N] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+                        }
+                    }
+                }
+                if (kCL > 1 && split > 1) {
+                    // slots read: let each sender write its next partial
+                    __syncwarp();
+                    if (lane == 0) {
+                        for (int k = 0; k < split; ++k) {
+                            if (k != krank) {
+                                ptx::mbar_arrive_remote(
+                                    ptx::mapa_shared(bar_tx_free + 8 * q, rank0 + k));
+                            }
+                        }
                     }
                 }
             }
@@ -420,16 +558,20 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_tempty + 8 * b);
         }
+        if (kCL > 1 && armed) {
+            // gave up while partials were on their way: let them land first
+            wait_drain(bar_rx_full + 8 * q, tc & 1u, timeout_ns);
+        }
     } else {
         // ------------------------------------------- scale staging -----
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;   // warps 2, 3, 8, 9, ...
         const int ws_row = K / 32;     // bytes per w_scale row
         uint32_t g = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+        for (int u = gid; ok && u < U; u += ngroups) {
             const Unit t = decode_unit(sch, u);
             const uint8_t* wsrc = w_scale + static_cast<size_t>(t.e * N + t.n0 + lane) * ws_row;
-            for (int ks = 0; ks < KT; ++ks, ++g) {
+            for (int ks = k0; ks < k1; ++ks, ++g) {
                 if (static_cast<int>(g % Cfg::kSfWarps) != sfw) continue;
                 const uint32_t slot = g % kStages;
                 const uint32_t ph = (g / kStages) & 1u;
@@ -475,7 +617,12 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    if (kCL > 1) {
+        __syncwarp();
+        ptx::cluster_sync();   // no CTA leaves while others may still write to it
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
@@ -844,24 +991,121 @@ __global__ void selftest_wait_kernel(uint32_t* status, uint64_t timeout_ns) {
     __syncthreads();
 }
 
+// Upper bound on the units of a launch: every non-empty expert needs at most
+// ceil(rows_e / T) token tiles <= rows_e / T + 1, times its weight tiles.
+long long units_upper(const GemmArgs& a, int t_max, int weight_rows_per_unit) {
+    const long long nt = a.N / weight_rows_per_unit;
+    const long long active = a.E < a.rows ? a.E : a.rows;
+    return ((a.rows + t_max - 1) / t_max + active) * nt;
+}
+
+// The occupancy calculator counts any kernel that uses tcgen05 as one CTA
+// per SM (measured on GB300: a 320-thread kernel with 100 KB of shared memory
+// reads 2 blocks per SM, 1 once it allocates TMEM, while 2 CTAs are resident
+// in both cases).  Cluster residency is therefore asked about this stand-in,
+// which has the GEMM kernel's block size, shared memory and minimum blocks
+// per SM; each GEMM CTA allocates 512 / C TMEM columns, so TMEM never limits
+// residency below C per SM.
+template <int kThreads, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) occupancy_stand_in() {}
+
+// Largest number of clusters of `cl` CTAs of `fn` that are resident at once
+// (clusters are placed whole inside a GPC, so this can be below
+// num_sms * ctas_per_sm / cl).  Cached per kernel, device and shared-memory
+// size; 0 when the query fails.
+int resident_clusters(const void* fn, int cl, int threads, size_t smem, bool attr_cluster) {
+    struct Entry {
+        const void* fn;
+        int dev;
+        int cl;
+        size_t smem;
+        int value;
+    };
+    static Entry cache[32];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        if (cache[i].fn == fn && cache[i].dev == dev && cache[i].cl == cl && cache[i].smem == smem) {
+            return cache[i].value;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    if (attr_cluster) {
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    if (used < 32) cache[used++] = Entry{fn, dev, cl, smem, n};
+    return n;
+}
+
+template <class Kern>
+cudaError_t set_smem_attr(Kern* fn, size_t bytes) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes));
+}
+
+// CTAs one launch uses (0: nothing to do).  Persistent grids: C CTAs per SM,
+// as whole clusters and no more clusters than can be resident at once (a
+// second wave would idle most of the GPU while it runs), and no more CTAs
+// than units (split-K clusters: CL CTAs per unit).
+template <class Cfg>
+long long grid_plain(const GemmArgs& a) {
+    long long grid = static_cast<long long>(a.num_sms) * Cfg::kCtasPerSm;
+    const long long u = units_upper(a, Cfg::kTMax, kBW);
+    return u < grid ? u : grid;
+}
+
+template <class Cfg>
+long long grid_cluster(const GemmArgs& a) {
+    constexpr int CL = Cfg::kCluster;
+    auto* stand_in = occupancy_stand_in<Cfg::kThreads, Cfg::kCtasPerSm>;
+    static cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
+    static cudaError_t attr_s = set_smem_attr(stand_in, kSmemPerBlockMax);
+    if (attr != cudaSuccess || attr_s != cudaSuccess) return 0;
+    long long grid = static_cast<long long>(a.num_sms) * Cfg::kCtasPerSm / CL * CL;
+    const int res = resident_clusters(reinterpret_cast<const void*>(stand_in), CL, Cfg::kThreads,
+                                      Cfg::smem_bytes(a.E), true);
+    if (res > 0 && static_cast<long long>(res) * CL < grid) grid = static_cast<long long>(res) * CL;
+    const long long u = units_upper(a, Cfg::kTMax, kBW) * CL;
+    return u < grid ? u : grid;
+}
+
+template <class Cfg>
+long long grid_pair(const GemmArgs& a) {
+    auto* stand_in = occupancy_stand_in<Cfg::kThreads, Cfg::kCtasPerSm>;
+    static cudaError_t attr = set_smem_attr(grouped_w4a8_pair_kernel<Cfg>, Cfg::smem_bytes(kMaxE));
+    static cudaError_t attr_s = set_smem_attr(stand_in, kSmemPerBlockMax);
+    if (attr != cudaSuccess || attr_s != cudaSuccess) return 0;
+    long long pairs = static_cast<long long>(a.num_sms / 2) * Cfg::kCtasPerSm;
+    const int res = resident_clusters(reinterpret_cast<const void*>(stand_in), 2, Cfg::kThreads,
+                                      Cfg::smem_bytes(a.E), true);
+    if (res > 0 && res < pairs) pairs = res;
+    const long long u = units_upper(a, Cfg::kTMax, 2 * kBW);
+    return 2 * (u < pairs ? u : pairs);
+}
+
 template <class Cfg>
 cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
                        const CUtensorMap& map_a64, cudaStream_t stream) {
-    static bool configured = false;   // the attribute is per kernel, process-wide
-    if (!configured) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_w4a8_kernel<Cfg>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(Cfg::smem_bytes(Cfg::kMaxExperts)));
-        if (err != cudaSuccess) return err;
-        configured = true;
-    }
-    // Upper bound on the number of units: every non-empty expert needs at
-    // most ceil(rows_e / T) token tiles <= rows_e / T + 1.
-    const long long nt = a.N / kBW;
-    const long long active = a.E < a.rows ? a.E : a.rows;
-    const long long units_max = ((a.rows + Cfg::kTMax - 1) / Cfg::kTMax + active) * nt;
-    long long grid = static_cast<long long>(a.num_sms) * Cfg::kCtasPerSm;
-    if (units_max < grid) grid = units_max;
+    static cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
+    if (attr != cudaSuccess) return attr;
+    const long long grid = grid_plain<Cfg>(a);
     if (grid < 1) return cudaSuccess;
     grouped_w4a8_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
                                stream>>>(map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets,
@@ -870,25 +1114,37 @@ cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtens
     return cudaGetLastError();
 }
 
+// Split-K variant: clusters of Cfg::kCluster CTAs, launched with the cluster
+// size as a launch attribute.
+template <class Cfg>
+cudaError_t launch_cluster(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
+                           const CUtensorMap& map_a64, cudaStream_t stream) {
+    const long long grid = grid_cluster<Cfg>(a);
+    if (grid < Cfg::kCluster) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::smem_bytes(a.E);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Cfg::kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_w4a8_kernel<Cfg>, map_w, map_a, map_a64, a.a_scale,
+                              a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out,
+                              a.status, a.timeout_ns);
+}
+
 template <class Cfg>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
                         const CUtensorMap& map_a64, cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_w4a8_pair_kernel<Cfg>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(Cfg::smem_bytes(kMaxE)));
-        if (err != cudaSuccess) return err;
-        configured = true;
-    }
-    const long long nt = a.N / (2 * kBW);
-    const long long active = a.E < a.rows ? a.E : a.rows;
-    const long long units_max = ((a.rows + Cfg::kTMax - 1) / Cfg::kTMax + active) * nt;
-    long long pairs = static_cast<long long>(a.num_sms / 2) * Cfg::kCtasPerSm;
-    if (units_max < pairs) pairs = units_max;
-    if (pairs < 1) return cudaSuccess;
-    grouped_w4a8_pair_kernel<Cfg><<<static_cast<int>(2 * pairs), Cfg::kThreads,
-                                    Cfg::smem_bytes(a.E), stream>>>(
+    const long long grid = grid_pair<Cfg>(a);
+    if (grid < 2) return cudaSuccess;
+    grouped_w4a8_pair_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
+                                    stream>>>(
         map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs,
         a.as_ks, a.out, a.status, a.timeout_ns);
     return cudaGetLastError();
@@ -903,17 +1159,43 @@ int gemm_variant_max_experts(int variant) {
         case 1: return CfgSmall::kMaxExperts;
         case 2: return CfgMid::kMaxExperts;
         case 3: return CfgLarge::kMaxExperts;
+        case 6: return CfgSplit::kMaxExperts;
         default: return kMaxE;
     }
 }
 
 // Variant choice from the mean rows per expert (the per-expert counts live on
 // the device).  Few rows: weight streaming dominates and two small pipelines
-// per SM keep the MMA issue rate up; many rows: the widest token tile.
-int gemm_pick_variant(int32_t E, int32_t N, int32_t rows) {
-    (void)N;
+// per SM keep the MMA issue rate up; many rows: the widest token tile.  With
+// at most 32 rows per expert the split-K variant is taken when, counting one
+// token tile per active expert (at most min(E, rows) of them), it leaves the
+// busiest CTA at least 15 % fewer stages than variant 1 (num_sms = 0: no
+// device to ask, never).
+int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms) {
     const long long per = rows / (E > 0 ? E : 1);
-    if (per <= 48) return 1;
+    if (per <= 48) {
+        if (num_sms > 0 && rows <= 32LL * E && K >= 512 && N >= kBW) {
+            GemmArgs a{};
+            a.E = E;
+            a.N = N;
+            a.K = K;
+            a.rows = 1 << 30;      // grid not capped by the unit count
+            a.num_sms = num_sms;
+            const long long g6 = grid_cluster<CfgSplit>(a);
+            const long long g1 = static_cast<long long>(num_sms) * CfgSmall::kCtasPerSm;
+            const long long units = static_cast<long long>(E < rows ? E : rows) * (N / kBW);
+            const int KT = K / kBK;
+            if (g6 >= CfgSplit::kCluster && units > 0) {
+                const long long c1 = (units + g1 - 1) / g1 * KT;
+                const int s = choose_split(static_cast<int>(units), KT, static_cast<int>(g6),
+                                           CfgSplit::kCluster);
+                const long long groups = g6 / s;
+                const long long c6 = (units + groups - 1) / groups * (KT / s);
+                if (20 * c6 <= 17 * c1) return 6;
+            }
+        }
+        return 1;
+    }
     if (per <= 640) return 2;
     return 3;
 }
@@ -925,6 +1207,7 @@ int gemm_variant_token_tile(int variant) {
         case 3: return CfgLarge::kTMax;
         case 4: return CfgPair::kTMax;
         case 5: return CfgPairMid::kTMax;
+        case 6: return CfgSplit::kTMax;
         default: return 0;
     }
 }
@@ -935,7 +1218,19 @@ size_t gemm_smem_bytes(int variant, int32_t E) {
         case 2: return CfgMid::smem_bytes(E);
         case 4: return CfgPair::smem_bytes(E);
         case 5: return CfgPairMid::smem_bytes(E);
+        case 6: return CfgSplit::smem_bytes(E);
         default: return CfgLarge::smem_bytes(E);
+    }
+}
+
+long long gemm_launch_ctas(const GemmArgs& a) {
+    switch (a.variant) {
+        case 1: return grid_plain<CfgSmall>(a);
+        case 2: return grid_plain<CfgMid>(a);
+        case 4: return grid_pair<CfgPair>(a);
+        case 5: return grid_pair<CfgPairMid>(a);
+        case 6: return grid_cluster<CfgSplit>(a);
+        default: return grid_plain<CfgLarge>(a);
     }
 }
 
@@ -947,6 +1242,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
         case 2: return launch_cfg<CfgMid>(a, map_w, map_a, map_a64, stream);
         case 4: return launch_pair<CfgPair>(a, map_w, map_a, map_a64, stream);
         case 5: return launch_pair<CfgPairMid>(a, map_w, map_a, map_a64, stream);
+        case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, map_a64, stream);
         default: return launch_cfg<CfgLarge>(a, map_w, map_a, map_a64, stream);
     }
 }

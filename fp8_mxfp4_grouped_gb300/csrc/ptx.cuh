@@ -209,6 +209,19 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Store 16 bytes into the shared memory of a CTA of the cluster and count
+// them against an mbarrier of that same CTA (complete_tx); both operands are
+// shared::cluster addresses.  The receiver sees the data once the barrier's
+// phase completes, with no fence on either side.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d, uint32_t cluster_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(cluster_addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+        : "memory");
+}
+
 // try_wait with acquire at cluster scope: for barriers other CTAs arrive on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;

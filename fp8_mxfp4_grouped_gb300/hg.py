@@ -53,6 +53,8 @@ lib.hg_set_wait_timeout_us.argtypes = [_u32]
 lib.hg_set_wait_timeout_us.restype = None
 lib.hg_gemm_token_tile.argtypes = [_i32, _i32, _i32, _i32]
 lib.hg_gemm_token_tile.restype = _i32
+lib.hg_gemm_ctas.argtypes = [_i32, _i32, _i32, _i32]
+lib.hg_gemm_ctas.restype = _i32
 lib.hg_set_gemm_variant.argtypes = [_i32]
 lib.hg_set_gemm_variant.restype = _i32
 
@@ -206,6 +208,10 @@ def hg_set_wait_timeout_us(timeout_us: int):
 
 def hg_gemm_token_tile(E: int, N: int, K: int, rows: int) -> int:
     return int(lib.hg_gemm_token_tile(E, N, K, rows))
+
+
+def hg_gemm_ctas(E: int, N: int, K: int, rows: int) -> int:
+    return int(lib.hg_gemm_ctas(E, N, K, rows))
 
 
 def hg_set_gemm_variant(variant: int) -> int:

@@ -20,16 +20,33 @@ T_MAX depends on the pipeline variant the library picks from rows / E
 from __future__ import annotations
 
 T_MAX = 224
-VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96}
-VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32}   # CTA pairs split the token tile in two
+VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96, 6: 32}
+VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32, 6: 16}   # CTA pairs split the token tile in two
+SPLIT_CLUSTER = 4        # variant 6: clusters of 4 CTAs, two per SM
 MMA_N_STEP = 16
 W_TILE = 128
 
 
-def pick_variant(E: int, N: int, rows: int) -> int:
-    """Mirror of the library's variant choice (mean rows per expert)."""
+def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
+                 split_ctas: int = 0) -> int:
+    """Mirror of the library's variant choice (mean rows per expert).
+
+    With a device (num_sms > 0, split_ctas = the split-K variant's resident
+    CTAs) and at most 32 rows per expert, variant 6 is taken when, counting
+    one token tile per active expert, it leaves the busiest CTA at least 15 %
+    fewer stages than variant 1."""
     per = rows // max(E, 1)
     if per <= 48:
+        if num_sms > 0 and rows <= 32 * E and K >= 512 and N >= W_TILE and split_ctas >= SPLIT_CLUSTER:
+            units = min(E, rows) * (N // W_TILE)
+            KT = K // 128
+            if units > 0:
+                g1 = num_sms * 2
+                c1 = -(-units // g1) * KT
+                s = choose_split(units, KT, split_ctas)
+                c6 = -(-units // (split_ctas // s)) * (KT // s)
+                if 20 * c6 <= 17 * c1:
+                    return 6
         return 1
     if per <= 640:
         return 2
@@ -68,3 +85,26 @@ def units(offsets, N: int, t_max: int = T_MAX):
             for (r0, valid, mma_n) in tiles:
                 out.append((e, nt * W_TILE, lo + r0, valid, mma_n))
     return out
+
+
+def choose_split(U: int, KT: int, G: int, max_split: int = SPLIT_CLUSTER) -> int:
+    """Mirror of the split-K factor variant 6 takes on the device: with G CTAs
+    and U units of KT stages, the s in {1, 2, 4} that minimises the stages of
+    the busiest CTA, ceil(U / (G / s)) * KT / s; ties keep the smaller s."""
+    best, best_cost = 1, -(-U // G) * KT
+    s = 2
+    while s <= max_split:
+        c = -(-U // (G // s)) * (KT // s)
+        if c < best_cost:
+            best, best_cost = s, c
+        s *= 2
+    return best
+
+
+def split_grid(num_sms: int, E: int, N: int, rows: int) -> int:
+    """CTAs variant 6 launches: two per SM in whole clusters, capped so that
+    every unit can be split four ways."""
+    t = VARIANT_T_MAX[6]
+    units_max = (-(-rows // t) + min(E, rows)) * (N // W_TILE)
+    grid = num_sms * 2 // SPLIT_CLUSTER * SPLIT_CLUSTER
+    return min(grid, units_max * SPLIT_CLUSTER)

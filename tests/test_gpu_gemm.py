@@ -17,7 +17,7 @@ from tests.gpu_util import assert_rows_close, bf16_bits, np_u8
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [1, 2, 3, 4, 5]   # see hg_set_gemm_variant
+VARIANTS = [1, 2, 3, 4, 5, 6]   # see hg_set_gemm_variant
 
 
 @pytest.fixture(params=VARIANTS, ids=lambda v: f"variant{v}")
@@ -175,6 +175,66 @@ def test_wait_timeout_is_reported_and_context_survives(cuda_lib):
     assert st == cuda_lib.HG_ERR_TIMEOUT
     assert (detail >> 24) == 6
     test_config0_full(cuda_lib)
+
+
+# --------------------------------------------------------- split-K (variant 6) --
+
+@pytest.mark.parametrize("want", [1, 2, 4])
+def test_split_k_each_factor(cuda_lib, want):
+    # experts of 1..32 rows (one token tile each) in numbers that make the
+    # device pick each split factor for this GPU's resident CTA count
+    from fp8_mxfp4_grouped_gb300 import tiles as T
+    N, K = 512, 2048
+    NT, KT = N // 128, K // 128
+    prev = cuda_lib.hg_set_gemm_variant(6)
+    try:
+        full = cuda_lib.hg_gemm_ctas(512, N, K, 1 << 20)          # grid with units to spare
+        assert full > 0 and full % 4 == 0
+        E = {1: full, 2: full * 3 // 2, 4: full // 4}[want] // NT
+        rng = np.random.default_rng(want)
+        cuts = np.concatenate([[0], np.cumsum(rng.integers(1, 33, E))]).astype(np.int32)
+        R = int(cuts[-1])
+        a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+        grid = cuda_lib.hg_gemm_ctas(E, N, K, R)
+        assert grid == min(full, T.split_grid(10 ** 6, E, N, R))
+        assert T.choose_split(E * NT, KT, grid) == want, grid
+        o1 = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
+        o2 = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
+    finally:
+        cuda_lib.hg_set_gemm_variant(prev)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K)
+    assert_rows_close(bf16_bits(o1), ref, f"split {want}")
+    assert np.array_equal(bf16_bits(o1), bf16_bits(o2))       # fixed summation order
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def test_split_k_auto_choice(cuda_lib):
+    # the library's choice on this device equals the host mirror's, and the
+    # six-expert-wide W13 projection at one token takes the split variant
+    from fp8_mxfp4_grouped_gb300 import tiles as T
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    prev = cuda_lib.hg_set_gemm_variant(6)
+    try:
+        split_ctas = cuda_lib.hg_gemm_ctas(12, 6144, 3584, 1 << 20)
+    finally:
+        cuda_lib.hg_set_gemm_variant(prev)
+    assert split_ctas > 0
+    for E, N, K, rows in [(12, 6144, 3584, 8), (12, 3584, 3072, 8), (12, 6144, 3584, 32),
+                          (12, 3584, 3072, 32), (32, 4096, 6144, 512), (4, 256, 512, 32),
+                          (12, 6144, 3584, 512), (32, 4096, 6144, 16384)]:
+        v = T.pick_variant(E, N, rows, K, sms, split_ctas)
+        assert cuda_lib.hg_gemm_token_tile(E, N, K, rows) == T.VARIANT_T_MAX[v], (E, N, K, rows)
+    assert T.pick_variant(12, 6144, 8, 3584, sms, split_ctas) == 6
+
+
+@pytest.mark.parametrize("proj", ["w13", "w2"])
+@pytest.mark.parametrize("M", [1, 8])
+def test_split_k_config3_small_m(cuda_lib, M, proj):
+    prev = cuda_lib.hg_set_gemm_variant(6)
+    try:
+        test_config3_small_m_full(cuda_lib, M, proj)
+    finally:
+        cuda_lib.hg_set_gemm_variant(prev)
 
 
 # ------------------------------------------------ full-size sampled parity --

@@ -73,3 +73,22 @@ def test_units_enumeration():
     us = T.units(off, 256)
     assert len(us) == 2 * (1 + 2)
     assert {u[0] for u in us} == {0, 2}
+
+
+@pytest.mark.parametrize("U,KT,G,want", [
+    (304, 16, 304, 1),     # one unit per CTA: nothing to even out
+    (456, 16, 304, 2),     # 1.5 units per CTA: halves even out (quarters tie, keep 2)
+    (76, 16, 304, 4),      # a quarter unit per CTA
+    (384, 28, 304, 2),     # 384 weight tiles of 28 stages (six-expert-wide W13 at M=1)
+    (224, 24, 304, 4),     # W2 at M=1: 224 tiles of 24 stages
+    (608, 48, 304, 1),     # exactly two per CTA
+    (0, 8, 304, 1),
+])
+def test_split_choice(U, KT, G, want):
+    assert T.choose_split(U, KT, G) == want
+    # brute force: the chosen split gives the least work on the busiest CTA
+    def busiest(s):
+        return max(len(range(g, U, G // s)) for g in range(G // s)) * (KT // s) if U else 0
+    costs = {s: busiest(s) for s in (1, 2, 4)}
+    assert costs[want] == min(costs.values())
+    assert all(costs[s] > costs[want] for s in (1, 2, 4) if s < want)
