@@ -347,13 +347,19 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     const WaitCtx wctx{status, misc + 1, timeout_ns};
     // Split-K: groups of `split` consecutive CTAs (inside one cluster) share
     // each unit, CTA krank of a group taking stages [k0, k1).  Every CTA
-    // derives the same split from U.
-    const int split = kCL > 1 ? choose_split(U, KT, static_cast<int>(gridDim.x), kCL) : 1;
-    const int krank = kCL > 1 ? static_cast<int>(blockIdx.x) % split : 0;
-    const int gid = static_cast<int>(blockIdx.x) / split;
-    const int ngroups = static_cast<int>(gridDim.x) / split;
-    const int k0 = krank * (KT / split);
-    const int k1 = k0 + KT / split;
+    // derives the same split from U.  Without clusters the loops below read
+    // blockIdx / gridDim / 0 / KT directly: holding the group geometry in
+    // registers across the warp roles slowed the single MMA-issuing thread
+    // by 15-19 % at large M (measured on GB300).
+    int split = 1, krank = 0, gid = 0, ngroups = 1, k0 = 0, k1 = KT;
+    if constexpr (kCL > 1) {
+        split = choose_split(U, KT, static_cast<int>(gridDim.x), kCL);
+        krank = static_cast<int>(blockIdx.x) % split;
+        gid = static_cast<int>(blockIdx.x) / split;
+        ngroups = static_cast<int>(gridDim.x) / split;
+        k0 = krank * (KT / split);
+        k1 = k0 + KT / split;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
@@ -362,12 +368,13 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             const uint64_t pol_a = ptx::policy_evict_last();
             uint32_t g = 0;
             bool ok = true;
-            for (int u = gid; ok && u < U; u += ngroups) {
+            for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
+                 u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x)) {
                 const Unit t = decode_unit(sch, u);
                 const int wrow = t.e * N + t.n0;
                 const int nbig = t.n_mma / kABigRows;
                 const int nsmall = (t.n_mma - nbig * kABigRows) / kABoxRows;
-                for (int ks = k0; ks < k1; ++ks, ++g) {
+                for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
                     if (!wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleProducer, slot)) {
@@ -402,7 +409,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         if (lane == 0) {
             uint32_t g = 0, tc = 0;
             bool ok = true;
-            for (int u = gid; ok && u < U; u += ngroups, ++tc) {
+            for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
+                 u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x), ++tc) {
                 const Unit t = decode_unit(sch, u);
                 const uint32_t b = tc & 1u;
                 if (!wait_bounded(bar_tempty + 8 * b, ((tc >> 1) & 1u) ^ 1u, wctx, kRoleMma,
@@ -413,7 +421,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 const uint32_t idesc0 =
                     ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, kBW, t.n_mma);
                 const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
-                for (int ks = k0; ks < k1; ++ks, ++g) {
+                for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
                     if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
@@ -437,7 +445,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                         ptx::mma_mxf8f6f4_1x(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
                                              ptx::desc_kmajor_sw128(asm_ + kk * 32),
                                              ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
-                                             sf_col + 4, (ks != k0 || kk != 0) ? 1u : 0u);
+                                             sf_col + 4, (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
                     }
                     ptx::tc_commit(bar_empty + 8 * slot);
                 }
@@ -464,14 +472,30 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             sbase + Cfg::kOffRx + (q - owner * per_owner) * (split - 1) * Cfg::kRxSlotBytes;
         uint32_t tc = 0;
         bool armed = false;   // a receive was announced and not yet seen complete
-        for (int u = gid; u < U; u += ngroups, ++tc) {
+        for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); u < U;
+             u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x), ++tc) {
             const Unit t = decode_unit(sch, u);
             const uint32_t b = tc & 1u;
             if (!wait_bounded(bar_tfull + 8 * b, (tc >> 1) & 1u, wctx, kRoleEpilogue, b)) break;
             ptx::tc_fence_after();
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
-            if (kCL > 1 && !finalise) {
+            if constexpr (kCL == 1) {
+                const int n = t.n0 + 32 * q + lane;
+                uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
+                for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+                    uint32_t v[16];
+                    ptx::tmem_ld_32x32b_x16(taddr + c0, v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (c0 + j < t.nrows) {
+                            dst[static_cast<size_t>(c0 + j) * N] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                        }
+                    }
+                }
+            } else if (!finalise) {
                 // ---- send this quadrant's partial to its owner
                 if (!wait_bounded<true>(bar_tx_free + 8 * q, (tc & 1u) ^ 1u, wctx, kRoleEpilogue,
                                         0x200u | q)) {
@@ -568,10 +592,11 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         const int ws_row = K / 32;     // bytes per w_scale row
         uint32_t g = 0;
         bool ok = true;
-        for (int u = gid; ok && u < U; u += ngroups) {
+        for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
+                 u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x)) {
             const Unit t = decode_unit(sch, u);
             const uint8_t* wsrc = w_scale + static_cast<size_t>(t.e * N + t.n0 + lane) * ws_row;
-            for (int ks = k0; ks < k1; ++ks, ++g) {
+            for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
                 if (static_cast<int>(g % Cfg::kSfWarps) != sfw) continue;
                 const uint32_t slot = g % kStages;
                 const uint32_t ph = (g / kStages) & 1u;
@@ -743,8 +768,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     const int U = s_prefix[E];
     const int KT = K / kBK;
     const WaitCtx wctx{status, misc + 1, timeout_ns};
-    const int pair = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
+    // Units u = blockIdx.x / 2 + i * gridDim.x / 2.  The loops read blockIdx
+    // and gridDim directly (see the note in grouped_w4a8_kernel on the
+    // single-thread roles' sensitivity to values held across them).
 
     // Unit geometry for this CTA of the pair.
     auto unit_of = [&](int u, int& e, int& wrow0, int& row0, int& nrows, int& n_mma) {
@@ -772,7 +798,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
             const uint64_t pol_a = ptx::policy_evict_last();
             uint32_t g = 0;
             bool ok = true;
-            for (int u = pair; ok && u < U; u += npairs) {
+            for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
+                 u += static_cast<int>(gridDim.x >> 1)) {
                 int e, wrow0, row0, nrows, n_mma;
                 unit_of(u, e, wrow0, row0, nrows, n_mma);
                 const int half = n_mma / 2;
@@ -813,7 +840,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
             // --------------------------------------- MMA issuer (pair) ---
             uint32_t g = 0, tc = 0;
             bool ok = true;
-            for (int u = pair; ok && u < U; u += npairs, ++tc) {
+            for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
+                 u += static_cast<int>(gridDim.x >> 1), ++tc) {
                 int e, wrow0, row0, nrows, n_mma;
                 unit_of(u, e, wrow0, row0, nrows, n_mma);
                 const uint32_t b = tc & 1u;
@@ -866,7 +894,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         const int q = warp & 3;
         const uint32_t tempty_leader = ptx::mapa_shared(bar_tempty, 0);
         uint32_t tc = 0;
-        for (int u = pair; u < U; u += npairs, ++tc) {
+        for (int u = static_cast<int>(blockIdx.x >> 1); u < U;
+             u += static_cast<int>(gridDim.x >> 1), ++tc) {
             int e, wrow0, row0, nrows, n_mma;
             unit_of(u, e, wrow0, row0, nrows, n_mma);
             const uint32_t b = tc & 1u;
@@ -901,7 +930,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         const uint32_t peer_bar0 = ptx::mapa_shared(bar_peer, 0);
         uint32_t g = 0;
         bool ok = true;
-        for (int u = pair; ok && u < U; u += npairs) {
+        for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
+                 u += static_cast<int>(gridDim.x >> 1)) {
             int e, wrow0, row0, nrows, n_mma;
             unit_of(u, e, wrow0, row0, nrows, n_mma);
             const uint8_t* wsrc =
