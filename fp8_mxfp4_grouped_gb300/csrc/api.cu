@@ -200,7 +200,8 @@ hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scal
 
     // Weights: [E*N rows, K elements] of E2M1, unpacked by the TMA into one
     // 16-byte chunk (8 data bytes + 8 pad) per 16 elements, 128-byte swizzle.
-    CUtensorMap map_w, map_a, map_a64;
+    CUtensorMap map_w;
+    AMaps map_a;
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K),
                               static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
@@ -213,13 +214,14 @@ hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scal
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return HG_ERR_CUDA;
     }
-    // Activations: [rows, K] bytes, 128-byte swizzle; 16-row and 64-row boxes.
-    for (int which = 0; which < 2; ++which) {
+    // Activations: [rows, K] bytes, 128-byte swizzle; boxes of 16, 32, 64 and
+    // 128 rows.
+    for (int which = 0; which < 4; ++which) {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-        cuuint32_t box[2] = {128, which == 0 ? 16u : 64u};
+        cuuint32_t box[2] = {128, 16u << which};
         cuuint32_t estr[2] = {1, 1};
-        if (encode(which == 0 ? &map_a : &map_a64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+        if (encode(&map_a.box[which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                    const_cast<uint8_t*>(a_fp8), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -243,7 +245,7 @@ hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scal
     a.timeout_ns = g_timeout_ns.load();
     a.num_sms = d->num_sms;
     a.variant = variant;
-    return launch_grouped_gemm(a, map_w, map_a, map_a64, reinterpret_cast<cudaStream_t>(stream)) ==
+    return launch_grouped_gemm(a, map_w, map_a, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? HG_OK
                : HG_ERR_CUDA;

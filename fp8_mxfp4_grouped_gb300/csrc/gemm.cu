@@ -36,14 +36,11 @@ namespace {
 constexpr int kBK = 128;              // K per pipeline stage = one activation-scale group
 constexpr int kBW = 128;              // weight rows per tile (MMA M)
 constexpr int kEpiWarps = 4;
-constexpr int kABoxRows = 16;         // rows per small activation TMA box
-constexpr int kABigRows = 64;         // rows per large activation TMA box
 constexpr int kMaxE = 512;            // scheduler tables live in shared memory
 constexpr uint32_t kWTileBytes = kBW * kBK;    // unpacked E2M1: one byte of smem per element
 // The 16U4_ALIGN16B TMA load writes 8 data bytes into each 16-byte chunk and
 // leaves the other 8 untouched; its transaction count is the packed bytes.
 constexpr uint32_t kWTileTx = kBW * kBK / 2;
-constexpr uint32_t kABigBytes = kABigRows * kBK;
 constexpr uint32_t kSfaBytes = 512;            // 128 rows x 4 blocks of 32 K
 constexpr uint32_t kSmemPerSm = 233472;        // 228 KB per SM on sm_103
 constexpr uint32_t kSmemPerBlockMax = 232448;  // 227 KB opt-in per block
@@ -97,7 +94,7 @@ struct GemmCfg {
         (static_cast<long long>(kSmemBudget) - static_cast<long long>(smem_bytes(0))) / 20 < kMaxE
             ? static_cast<int>((kSmemBudget - smem_bytes(0)) / 20)
             : kMaxE;
-    static_assert(T % 16 == 0 && T >= 16 && T <= 256, "MMA N");
+    static_assert(T % 16 == 0 && T >= 16 && T <= 240, "MMA N; at most four activation boxes");
     static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
     static_assert(kSfCol0 + S * kSfSlotCols <= kTmemCols, "TMEM budget");
     static_assert(kMaxExperts >= 32 && smem_bytes(kMaxExperts) <= kSmemBudget,
@@ -140,7 +137,7 @@ struct PairCfg {
     static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
     static_assert(kSfCol0 + S * kSfSlotCols <= kTmemCols, "TMEM budget");
     static_assert(smem_bytes(kMaxE) <= kSmemBudget, "shared memory budget");
-    static_assert(8 * (4 * S + 5) <= 256, "barrier area");
+    static_assert(8 * (3 * S + 5) <= 256, "barrier area");
     static_assert(C * 32 * (6 + S) * 96 <= 65536, "registers for C resident CTAs");
 };
 
@@ -228,11 +225,32 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
+// Load `n` activation rows (a multiple of 16, at most 240) starting at row
+// `row`, K offset `k`, into the swizzled tile at `dst`: one TMA per set bit
+// of n / 16, largest box first, so a tile takes at most four instructions.
+// kPair: the CTA-pair form, `bar` a shared::cluster address in either CTA.
+template <bool kPair = false>
+__device__ __forceinline__ void load_a_rows(const AMaps& maps, uint32_t dst, int k, int row, int n,
+                                            uint32_t bar, uint64_t policy) {
+    int r = 0;
+#pragma unroll
+    for (int i = 3; i >= 0; --i) {
+        const int h = 16 << i;
+        if (n & h) {
+            if (kPair) {
+                ptx::tma_load_2d_pair(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
+            } else {
+                ptx::tma_load_2d(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
+            }
+            r += h;
+        }
+    }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
 grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
-                    const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_a64,
+                    const __grid_constant__ AMaps map_a,
                     const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
                     const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
                     int as_rs, int as_ks, uint16_t* __restrict__ out, uint32_t* status,
@@ -291,8 +309,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&map_w);
-        ptx::prefetch_tensormap(&map_a);
-        ptx::prefetch_tensormap(&map_a64);
+        for (int i = 0; i < 4; ++i) ptx::prefetch_tensormap(&map_a.box[i]);
     }
 
     // Per-expert token tiling, from the expert's own row count.
@@ -372,8 +389,6 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                  u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x)) {
                 const Unit t = decode_unit(sch, u);
                 const int wrow = t.e * N + t.n0;
-                const int nbig = t.n_mma / kABigRows;
-                const int nsmall = (t.n_mma - nbig * kABigRows) / kABoxRows;
                 for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
@@ -385,16 +400,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     ptx::mbar_arrive_expect_tx(fb, kWTileTx + t.n_mma * kBK);
                     ptx::tma_load_2d(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w, ks * kBK,
                                      wrow, fb, pol_w);
-                    const uint32_t adst = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
-                    for (int j = 0; j < nbig; ++j) {
-                        ptx::tma_load_2d(adst + j * kABigBytes, &map_a64, ks * kBK,
-                                         t.row0 + j * kABigRows, fb, pol_a);
-                    }
-                    const int r0 = nbig * kABigRows;
-                    for (int j = 0; j < nsmall; ++j) {
-                        ptx::tma_load_2d(adst + (r0 + j * kABoxRows) * kBK, &map_a, ks * kBK,
-                                         t.row0 + r0 + j * kABoxRows, fb, pol_a);
-                    }
+                    load_a_rows(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes, ks * kBK,
+                                t.row0, t.n_mma, fb, pol_a);
                 }
             }
             // No copy may land after the CTA exits: wait for the last ring's
@@ -664,8 +671,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
 template <class Cfg>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
 grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
-                         const __grid_constant__ CUtensorMap map_a,
-                         const __grid_constant__ CUtensorMap map_a64,
+                         const __grid_constant__ AMaps map_a,
                          const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
                          const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
                          int as_rs, int as_ks, uint16_t* __restrict__ out, uint32_t* status,
@@ -682,10 +688,13 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     const uint32_t rank = ptx::cluster_ctarank();
     const bool leader = rank == 0;
 
+    // Leader (even CTA): bar_full_tma counts both CTAs' TMA bytes of a stage
+    // (the odd CTA's loads signal it directly), bar_full_sf takes one arrival
+    // from each CTA's scale warp.  bar_empty: in both CTAs, released by the
+    // leader's multicast commit.
     const uint32_t bar_full_tma = sbase + Cfg::kOffBar;
     const uint32_t bar_full_sf = bar_full_tma + 8 * kStages;
-    const uint32_t bar_peer = bar_full_sf + 8 * kStages;     // leader: the odd CTA's stage is loaded
-    const uint32_t bar_empty = bar_peer + 8 * kStages;
+    const uint32_t bar_empty = bar_full_sf + 8 * kStages;
     const uint32_t bar_tfull = bar_empty + 8 * kStages;
     const uint32_t bar_tempty = bar_tfull + 16;               // leader: both CTAs drained TMEM
     const uint32_t bar_done = bar_tempty + 16;
@@ -699,8 +708,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar_full_tma + 8 * s, 1);
-            ptx::mbar_init(bar_full_sf + 8 * s, 1);
-            ptx::mbar_init(bar_peer + 8 * s, 1);
+            ptx::mbar_init(bar_full_sf + 8 * s, 2);
             ptx::mbar_init(bar_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -717,8 +725,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&map_w);
-        ptx::prefetch_tensormap(&map_a);
-        ptx::prefetch_tensormap(&map_a64);
+        for (int i = 0; i < 4; ++i) ptx::prefetch_tensormap(&map_a.box[i]);
     }
 
     // Per-expert token tiling (tiles rounded to 32 rows: two halves of 16k).
@@ -796,6 +803,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         if (lane == 0) {
             const uint64_t pol_w = ptx::policy_evict_first();
             const uint64_t pol_a = ptx::policy_evict_last();
+            const uint32_t full_tma_leader = ptx::mapa_shared(bar_full_tma, 0);
             uint32_t g = 0;
             bool ok = true;
             for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
@@ -805,8 +813,6 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 const int half = n_mma / 2;
                 const int wrow = e * N + wrow0 + static_cast<int>(rank) * kBW;
                 const int arow = row0 + static_cast<int>(rank) * half;
-                const int nbig = half / kABigRows;
-                const int nsmall = (half - nbig * kABigRows) / kABoxRows;
                 for (int ks = 0; ks < KT; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
@@ -814,25 +820,26 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = bar_full_tma + 8 * slot;
-                    ptx::mbar_arrive_expect_tx(fb, kWTileTx + half * kBK);
-                    ptx::tma_load_2d(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w, ks * kBK,
-                                     wrow, fb, pol_w);
-                    const uint32_t adst = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
-                    for (int j = 0; j < nbig; ++j) {
-                        ptx::tma_load_2d(adst + j * kABigBytes, &map_a64, ks * kBK,
-                                         arow + j * kABigRows, fb, pol_a);
-                    }
-                    const int r0 = nbig * kABigRows;
-                    for (int j = 0; j < nsmall; ++j) {
-                        ptx::tma_load_2d(adst + (r0 + j * kABoxRows) * kBK, &map_a, ks * kBK,
-                                         arow + r0 + j * kABoxRows, fb, pol_a);
-                    }
+                    // both CTAs' bytes land on the leader's barrier
+                    const uint32_t fb = full_tma_leader + 8 * slot;
+                    if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * (kWTileTx + half * kBK));
+                    ptx::tma_load_2d_pair(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w,
+                                          ks * kBK, wrow, fb, pol_w);
+                    load_a_rows<true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
+                                      ks * kBK, arow, half, fb, pol_a);
                 }
             }
+            // No copy may land after the CTA exits.  The leader sees its
+            // stages complete on bar_full_tma; the odd CTA only through the
+            // leader's release of the slot (bar_empty), once it consumed it.
             const uint32_t first = g > kStages ? g - kStages : 0;
             for (uint32_t gg = first; gg < g; ++gg) {
-                wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
+                if (leader) {
+                    wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
+                } else {
+                    // the leader's commit of stage gg completes phase gg / S
+                    wait_drain(bar_empty + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
+                }
             }
         }
     } else if (warp == 1) {
@@ -856,9 +863,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 for (int ks = 0; ks < KT; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
-                    if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
-                        !wait_bounded(bar_full_sf + 8 * slot, ph, wctx, kRoleMma, 0x10u | slot) ||
-                        !wait_bounded<true>(bar_peer + 8 * slot, ph, wctx, kRoleMma, 0x20u | slot)) {
+                    if (!wait_bounded<true>(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
+                        !wait_bounded<true>(bar_full_sf + 8 * slot, ph, wctx, kRoleMma,
+                                            0x10u | slot)) {
                         ok = false;
                         break;
                     }
@@ -927,7 +934,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         // token tile (each CTA's TMEM needs all N columns' scales).
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;
         const int ws_row = K / 32;
-        const uint32_t peer_bar0 = ptx::mapa_shared(bar_peer, 0);
+        const uint32_t full_sf_leader = ptx::mapa_shared(bar_full_sf, 0);
         uint32_t g = 0;
         bool ok = true;
         for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
@@ -977,17 +984,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                     if (leader) {
                         ptx::mbar_arrive(bar_full_sf + 8 * slot);
                     } else {
-                        // The odd CTA's stage is complete once its own TMA
-                        // bytes have landed; publish both to the even CTA.
-                        if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleRelay, slot)) {
-                            ok = false;
-                        } else {
-                            ptx::mbar_arrive_remote(peer_bar0 + 8 * slot);
-                        }
+                        ptx::mbar_arrive_remote(full_sf_leader + 8 * slot);
                     }
                 }
-                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
             }
         }
     }
@@ -1131,14 +1130,14 @@ long long grid_pair(const GemmArgs& a) {
 }
 
 template <class Cfg>
-cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
-                       const CUtensorMap& map_a64, cudaStream_t stream) {
+cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
+                       cudaStream_t stream) {
     static cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
     if (attr != cudaSuccess) return attr;
     const long long grid = grid_plain<Cfg>(a);
     if (grid < 1) return cudaSuccess;
     grouped_w4a8_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
-                               stream>>>(map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets,
+                               stream>>>(map_w, map_a, a.a_scale, a.w_scale, a.offsets,
                                          a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out, a.status,
                                          a.timeout_ns);
     return cudaGetLastError();
@@ -1147,8 +1146,8 @@ cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const CUtens
 // Split-K variant: clusters of Cfg::kCluster CTAs, launched with the cluster
 // size as a launch attribute.
 template <class Cfg>
-cudaError_t launch_cluster(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
-                           const CUtensorMap& map_a64, cudaStream_t stream) {
+cudaError_t launch_cluster(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
+                           cudaStream_t stream) {
     const long long grid = grid_cluster<Cfg>(a);
     if (grid < Cfg::kCluster) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
@@ -1163,19 +1162,19 @@ cudaError_t launch_cluster(const GemmArgs& a, const CUtensorMap& map_w, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_w4a8_kernel<Cfg>, map_w, map_a, map_a64, a.a_scale,
+    return cudaLaunchKernelEx(&cfg, grouped_w4a8_kernel<Cfg>, map_w, map_a, a.a_scale,
                               a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out,
                               a.status, a.timeout_ns);
 }
 
 template <class Cfg>
-cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const CUtensorMap& map_a,
-                        const CUtensorMap& map_a64, cudaStream_t stream) {
+cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
+                        cudaStream_t stream) {
     const long long grid = grid_pair<Cfg>(a);
     if (grid < 2) return cudaSuccess;
     grouped_w4a8_pair_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
                                     stream>>>(
-        map_w, map_a, map_a64, a.a_scale, a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs,
+        map_w, map_a, a.a_scale, a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs,
         a.as_ks, a.out, a.status, a.timeout_ns);
     return cudaGetLastError();
 }
@@ -1264,16 +1263,15 @@ long long gemm_launch_ctas(const GemmArgs& a) {
     }
 }
 
-cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
-                                const CUtensorMap& map_a, const CUtensorMap& map_a64,
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
                                 cudaStream_t stream) {
     switch (a.variant) {
-        case 1: return launch_cfg<CfgSmall>(a, map_w, map_a, map_a64, stream);
-        case 2: return launch_cfg<CfgMid>(a, map_w, map_a, map_a64, stream);
-        case 4: return launch_pair<CfgPair>(a, map_w, map_a, map_a64, stream);
-        case 5: return launch_pair<CfgPairMid>(a, map_w, map_a, map_a64, stream);
-        case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, map_a64, stream);
-        default: return launch_cfg<CfgLarge>(a, map_w, map_a, map_a64, stream);
+        case 1: return launch_cfg<CfgSmall>(a, map_w, map_a, stream);
+        case 2: return launch_cfg<CfgMid>(a, map_w, map_a, stream);
+        case 4: return launch_pair<CfgPair>(a, map_w, map_a, stream);
+        case 5: return launch_pair<CfgPairMid>(a, map_w, map_a, stream);
+        case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, stream);
+        default: return launch_cfg<CfgLarge>(a, map_w, map_a, stream);
     }
 }
 

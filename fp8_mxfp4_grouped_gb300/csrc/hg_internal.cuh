@@ -85,8 +85,14 @@ struct GemmArgs {
     int variant;   // 1 small tiles / 2 CTAs per SM, 2 mid, 3 large tiles / 1 CTA per SM, 4 CTA pairs
 };
 
-cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w,
-                                const CUtensorMap& map_a, const CUtensorMap& map_a64,
+// Activation tensor maps over the same [rows, K] bytes, 128-byte swizzle,
+// with boxes of 128 K x (16 << i) rows: any multiple of 16 rows up to 240
+// loads in at most four boxes (one TMA instruction each).
+struct AMaps {
+    CUtensorMap box[4];
+};
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
                                 cudaStream_t stream);
 size_t gemm_smem_bytes(int variant, int32_t E);
 long long gemm_launch_ctas(const GemmArgs& a);   // CTAs the launch would use
