@@ -441,15 +441,19 @@ def time_moe_io(cs, flush, stream, peaks, hg, reps=20):
         return statistics.median(x0.elapsed_time(x1) for x0, x1 in ts) * 1e3
 
     tq = timed(lambda: hg.hg_quantize_gather_acts(x, k, b["s2d"], a, s, stream=stream))
+    tqs = timed(lambda: hg.hg_quantize_scatter_acts(x, k, b["d2s"], a, s, stream=stream))
     tc = timed(lambda: hg.hg_combine_topk(b["out"], b["d2s"], w, out, stream=stream))
-    bq = M * K * 2 + R * 4 + R * K + R * K / 128
+    bq = M * K * 2 + R * 4 + R * K + R * K / 128     # tokens read once, codes written once per row
     bc = R * N * 2 + R * 4 + M * k * 4 + M * N * 2
     hbm = peaks["hbm_gbs"]
-    return {"M": M, "quantize_gather_us": round(tq, 2), "quantize_gather_gbs": round(bq / tq / 1e3, 1),
+    return {"M": M, "quantize_scatter_us": round(tqs, 2),
+            "quantize_scatter_gbs": round(bq / tqs / 1e3, 1),
+            "quantize_scatter_roof_frac": round(bq / tqs / 1e3 / hbm, 3),
+            "quantize_gather_us": round(tq, 2), "quantize_gather_gbs": round(bq / tq / 1e3, 1),
             "quantize_gather_roof_frac": round(bq / tq / 1e3 / hbm, 3),
             "combine_us": round(tc, 2), "combine_gbs": round(bc / tc / 1e3, 1),
             "combine_roof_frac": round(bc / tc / 1e3 / hbm, 3),
-            "bytes": {"quantize_gather": int(bq), "combine": int(bc)}}
+            "bytes": {"quantize": int(bq), "combine": int(bc)}}
 
 
 # ------------------------------------------------------------ oracle arms --

@@ -292,6 +292,26 @@ hg_status hg_quantize_gather_acts(const uint16_t* x_bf16, int32_t M, int32_t K, 
                : HG_ERR_CUDA;
 }
 
+hg_status hg_quantize_scatter_acts(const uint16_t* x_bf16, int32_t M, int32_t K, int32_t top_k,
+                                   const int32_t* src_to_sorted, uint8_t* a_fp8,
+                                   uint8_t* a_scale, hg_stream_t stream) {
+    if (M < 0 || K < 1 || top_k < 1) return HG_ERR_INVALID_ARG;
+    if (K % 128 != 0 || top_k > quantize_scatter_max_top_k()) return HG_ERR_UNSUPPORTED_SHAPE;
+    const long long rows = static_cast<long long>(M) * top_k;
+    if (rows > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return HG_OK;
+    if (!x_bf16 || !src_to_sorted || !a_fp8 || !a_scale) return HG_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(a_fp8, 16)) return HG_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    hg_status st = device_info(&d);
+    if (st != HG_OK) return st;
+    return launch_quantize_scatter(x_bf16, M, K, top_k, src_to_sorted, static_cast<int>(rows),
+                                   a_fp8, a_scale, d->num_sms,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HG_OK
+               : HG_ERR_CUDA;
+}
+
 hg_status hg_combine_topk(const uint16_t* y_bf16, const int32_t* src_to_sorted,
                           const float* topk_weights, int32_t M, int32_t top_k, int32_t N,
                           uint16_t* out_bf16, hg_stream_t stream) {

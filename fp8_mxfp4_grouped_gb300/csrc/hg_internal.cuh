@@ -124,6 +124,10 @@ cudaError_t launch_selftest_wait(uint32_t* status, uint64_t timeout_ns, cudaStre
 cudaError_t launch_quantize_gather(const uint16_t* x, int K, int top_k, const int32_t* s2d,
                                    int rows, uint8_t* a_fp8, uint8_t* a_scale, int num_sms,
                                    cudaStream_t stream);
+cudaError_t launch_quantize_scatter(const uint16_t* x, int M, int K, int top_k, const int32_t* d2s,
+                                    int rows, uint8_t* a_fp8, uint8_t* a_scale, int num_sms,
+                                    cudaStream_t stream);
+int quantize_scatter_max_top_k();
 cudaError_t launch_combine_topk(const uint16_t* y, const int32_t* d2s, const float* weights,
                                 int M, int top_k, int N, uint16_t* out, int num_sms,
                                 cudaStream_t stream);

@@ -9,6 +9,9 @@
 //    rowwise MXFP8 cast of TransformerEngine PR #3459 ("non-TMA MXFP8
 //    cast-only kernels", description) is the same kind of register-only,
 //    HBM-bound cast, with 32-element blocks there and 128 here.
+//    hg_quantize_scatter_acts: the same codes, each token quantised once and
+//    stored to its top_k sorted rows src_to_sorted[t*k + j] (the plan's
+//    inverse permutation): the token is read once instead of top_k times.
 // 2. hg_combine_topk: out[t, :] = sum_j w[t, j] * y[src_to_sorted[t*k+j], :]
 //    in FP32, j ascending, rounded once to BF16; terms whose id was dropped
 //    by the plan (src_to_sorted = -1) are skipped.
@@ -52,8 +55,14 @@ constexpr int kQThreads = 256;
 constexpr int kQHalves = kQThreads / 16;
 constexpr int kQMaxIter = 4;                       // groups per half-warp held in registers
 
-__device__ __forceinline__ void quantize_group(const uint4 v, uint8_t* dst, uint8_t* scale_dst,
-                                               int j) {
+struct GroupCodes {
+    uint32_t lo, hi;        // this lane's 8 E4M3 codes
+    uint8_t scale;          // the group's E8M0 code
+};
+
+// Lane j of a half-warp holds elements 8j .. 8j+7 of one 128-element group;
+// every lane of the warp must call this (the amax reduction shuffles).
+__device__ __forceinline__ GroupCodes quantize_codes(const uint4 v) {
     float f[8];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -73,15 +82,13 @@ __device__ __forceinline__ void quantize_group(const uint4 v, uint8_t* dst, uint
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite ? 1 : 0, o) != 0;
     }
-    if (dst == nullptr) return;
-    uint8_t code_scale;
-    uint32_t lo, hi;
+    GroupCodes c;
     if (nonfinite) {
-        code_scale = 0xFF;                         // E8M0 NaN
-        lo = hi = 0x7F7F7F7Fu;                     // E4M3 NaN
+        c.scale = 0xFF;                            // E8M0 NaN
+        c.lo = c.hi = 0x7F7F7F7Fu;                 // E4M3 NaN
     } else {
         const int e = scale_exponent(amax);
-        code_scale = static_cast<uint8_t>(127 + e);
+        c.scale = static_cast<uint8_t>(127 + e);
         // 2^-e from its bits: finite BF16 inputs give e <= 120, so the
         // biased exponent 127 - e stays in [7, 254] (a normal float).
         const float inv = __int_as_float((127 - e) << 23);
@@ -90,11 +97,18 @@ __device__ __forceinline__ void quantize_group(const uint4 v, uint8_t* dst, uint
         for (int i = 0; i < 8; ++i) {
             b[i] = __nv_cvt_float_to_fp8(f[i] * inv, __NV_SATFINITE, __NV_E4M3);
         }
-        lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-        hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+        c.lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+        c.hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
     }
-    *reinterpret_cast<uint2*>(dst + 8 * j) = make_uint2(lo, hi);
-    if (j == 0) *scale_dst = code_scale;
+    return c;
+}
+
+__device__ __forceinline__ void quantize_group(const uint4 v, uint8_t* dst, uint8_t* scale_dst,
+                                               int j) {
+    const GroupCodes c = quantize_codes(v);
+    if (dst == nullptr) return;
+    *reinterpret_cast<uint2*>(dst + 8 * j) = make_uint2(c.lo, c.hi);
+    if (j == 0) *scale_dst = c.scale;
 }
 
 __global__ void __launch_bounds__(kQThreads)
@@ -126,6 +140,54 @@ quantize_gather_kernel(const uint16_t* __restrict__ x, int K, int top_k,
                 quantize_group(v[k], g < G ? arow + g * kGroup : nullptr, srow + g, j);
             }
         }
+    }
+}
+
+// One 256-thread block per token and pass: the token's destination rows are
+// read into shared memory, its groups are loaded and quantised once (as in
+// quantize_gather_kernel), and each half-warp stores its group's codes and
+// scale to every destination row in [0, rows).
+constexpr int kMaxScatterTopK = 64;
+
+__global__ void __launch_bounds__(kQThreads)
+quantize_scatter_kernel(const uint16_t* __restrict__ x, int M, int K, int top_k,
+                        const int32_t* __restrict__ src_to_sorted, int rows,
+                        uint8_t* __restrict__ a_fp8, uint8_t* __restrict__ a_scale) {
+    __shared__ int s_dst[kMaxScatterTopK];
+    const int G = K / kGroup;
+    const int hw = threadIdx.x >> 4;
+    const int j = threadIdx.x & 15;
+    for (int t = blockIdx.x; t < M; t += gridDim.x) {
+        if (threadIdx.x < top_k) {
+            const int r = __ldg(src_to_sorted + static_cast<long long>(t) * top_k + threadIdx.x);
+            s_dst[threadIdx.x] = (r >= 0 && r < rows) ? r : -1;
+        }
+        __syncthreads();
+        const uint16_t* xrow = x + static_cast<long long>(t) * K;
+        for (int g0 = 0; g0 < G; g0 += kQHalves * kQMaxIter) {
+            uint4 v[kQMaxIter];
+#pragma unroll
+            for (int k = 0; k < kQMaxIter; ++k) {
+                const int g = g0 + hw + kQHalves * k;
+                v[k] = make_uint4(0, 0, 0, 0);
+                if (g < G) v[k] = __ldg(reinterpret_cast<const uint4*>(xrow + g * kGroup) + j);
+            }
+#pragma unroll
+            for (int k = 0; k < kQMaxIter; ++k) {
+                const int g = g0 + hw + kQHalves * k;
+                const GroupCodes c = quantize_codes(v[k]);   // every lane: shuffles inside
+                if (g < G) {
+                    for (int d = 0; d < top_k; ++d) {
+                        const int r = s_dst[d];
+                        if (r < 0) continue;
+                        *reinterpret_cast<uint2*>(a_fp8 + static_cast<long long>(r) * K +
+                                                  g * kGroup + 8 * j) = make_uint2(c.lo, c.hi);
+                        if (j == 0) a_scale[static_cast<long long>(r) * G + g] = c.scale;
+                    }
+                }
+            }
+        }
+        __syncthreads();   // s_dst is rewritten for the next token
     }
 }
 
@@ -207,6 +269,20 @@ cudaError_t launch_quantize_gather(const uint16_t* x, int K, int top_k, const in
         x, K, top_k, s2d, rows, a_fp8, a_scale);
     return cudaGetLastError();
 }
+
+cudaError_t launch_quantize_scatter(const uint16_t* x, int M, int K, int top_k, const int32_t* d2s,
+                                    int rows, uint8_t* a_fp8, uint8_t* a_scale, int num_sms,
+                                    cudaStream_t stream) {
+    long long blocks = M;                            // one token per block and pass
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) return cudaSuccess;
+    quantize_scatter_kernel<<<static_cast<int>(blocks), kQThreads, 0, stream>>>(
+        x, M, K, top_k, d2s, rows, a_fp8, a_scale);
+    return cudaGetLastError();
+}
+
+int quantize_scatter_max_top_k() { return kMaxScatterTopK; }
 
 cudaError_t launch_combine_topk(const uint16_t* y, const int32_t* d2s, const float* weights,
                                 int M, int top_k, int N, uint16_t* out, int num_sms,

@@ -43,6 +43,8 @@ lib.hg_grouped_w4a8_gemm_mmajor.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32
 lib.hg_grouped_w4a8_gemm_mmajor.restype = ctypes.c_int
 lib.hg_quantize_gather_acts.argtypes = [_p, _i32, _i32, _i32, _p, _p, _p, _p]
 lib.hg_quantize_gather_acts.restype = ctypes.c_int
+lib.hg_quantize_scatter_acts.argtypes = [_p, _i32, _i32, _i32, _p, _p, _p, _p]
+lib.hg_quantize_scatter_acts.restype = ctypes.c_int
 lib.hg_combine_topk.argtypes = [_p, _p, _p, _i32, _i32, _i32, _p, _p]
 lib.hg_combine_topk.restype = ctypes.c_int
 lib.hg_get_device_status.argtypes = [_p, ctypes.POINTER(_u32)]
@@ -174,6 +176,23 @@ def hg_quantize_gather_acts(x_bf16: torch.Tensor, top_k: int, sorted_to_src: tor
     st = lib.hg_quantize_gather_acts(_ptr(x_bf16), M, K, top_k, _ptr(sorted_to_src), _ptr(a_fp8),
                                      _ptr(a_scale), _stream(stream))
     _check(st, "hg_quantize_gather_acts")
+    return a_fp8, a_scale
+
+
+def hg_quantize_scatter_acts(x_bf16: torch.Tensor, top_k: int, src_to_sorted: torch.Tensor,
+                             a_fp8=None, a_scale=None, stream=None):
+    """BF16 [M, K] tokens -> (E4M3 [M*top_k, K], E8M0 [M*top_k, K/128]); token t's codes
+    go to rows src_to_sorted[t*top_k + j]."""
+    assert x_bf16.dtype == torch.bfloat16 and x_bf16.is_contiguous() and x_bf16.dim() == 2
+    M, K = x_bf16.shape
+    R = M * top_k
+    if a_fp8 is None:
+        a_fp8 = torch.empty((R, K), dtype=torch.uint8, device=x_bf16.device)
+    if a_scale is None:
+        a_scale = torch.empty((R, K // 128), dtype=torch.uint8, device=x_bf16.device)
+    st = lib.hg_quantize_scatter_acts(_ptr(x_bf16), M, K, top_k, _ptr(src_to_sorted),
+                                      _ptr(a_fp8), _ptr(a_scale), _stream(stream))
+    _check(st, "hg_quantize_scatter_acts")
     return a_fp8, a_scale
 
 

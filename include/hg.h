@@ -236,6 +236,28 @@ hg_status hg_quantize_gather_acts(const uint16_t* x_bf16, int32_t M, int32_t K, 
                                   uint8_t* a_scale, hg_stream_t stream);
 
 /*
+ * The same quantisation as hg_quantize_gather_acts, organised per token:
+ * token t is read and quantised once, and its codes and scales are stored
+ * to the sorted rows src_to_sorted[t*top_k + j], j = 0 .. top_k-1 (the
+ * inverse permutation hg_plan_expert_offsets returns).  Entries outside
+ * [0, M*top_k) are skipped (ids the plan dropped are -1); rows no entry
+ * names are not written.  For a plan's pair of permutations the result is
+ * identical to hg_quantize_gather_acts, with each token read once instead
+ * of top_k times.
+ *
+ *   x_bf16         uint16 [M, K] BF16 bit patterns, 16-byte aligned.
+ *   src_to_sorted  int32 [M*top_k] from hg_plan_expert_offsets.
+ *   a_fp8          uint8 [M*top_k, K] out, 16-byte aligned; a_scale uint8 [M*top_k, K/128] out.
+ * K % 128 == 0; top_k <= 64 (else HG_ERR_UNSUPPORTED_SHAPE).  One kernel on
+ * `stream`; no host synchronisation.  The pages have no counterpart to the
+ * per-token organisation; it moves the same bytes as the gather with each
+ * token read once.
+ */
+hg_status hg_quantize_scatter_acts(const uint16_t* x_bf16, int32_t M, int32_t K, int32_t top_k,
+                                   const int32_t* src_to_sorted, uint8_t* a_fp8,
+                                   uint8_t* a_scale, hg_stream_t stream);
+
+/*
  * Combine the experts' outputs back into token order with the router's top-k
  * weights: out[t, :] = bf16_rne( sum_j w[t, j] * y[src_to_sorted[t*top_k + j], :] ),
  * the sum in FP32 over j ascending; terms with src_to_sorted < 0 (ids the

@@ -19,7 +19,8 @@ that they be covered): a group holding an Inf or a NaN gets scale code 0xFF
 and element codes 0x7F -- the NaN codes of E8M0 and E4M3.
 
 Gather: sorted row r holds token sorted_to_src[r] // top_k (rows with a
-negative source stay untouched).
+negative source stay untouched).  Scatter: token t goes to the rows
+src_to_sorted[t*top_k + j] (entries outside [0, M*top_k) skipped).
 
 Combine: out[t, :] = bf16_rne( sum_j w[t, j] * y[src_to_sorted[t*k + j], :] ),
 exact sum in float64, terms with src_to_sorted < 0 skipped.
@@ -98,6 +99,23 @@ def quantize_gather(x_bf16_bits, top_k: int, sorted_to_src, a_fp8_init=None, a_s
     ok = s2d >= 0
     a[ok] = codes[s2d[ok] // top_k]
     s[ok] = scales[s2d[ok] // top_k]
+    return a, s
+
+
+def quantize_scatter(x_bf16_bits, top_k: int, src_to_sorted, a_fp8_init=None, a_scale_init=None):
+    """Quantise each token once, then store it to rows src_to_sorted[t*top_k + j]
+    (entries outside [0, M*top_k) skipped)."""
+    codes, scales = quantize_rows(x_bf16_bits)
+    d2s = np.asarray(src_to_sorted, dtype=np.int64)
+    M, K = codes.shape
+    R = M * top_k
+    a = np.zeros((R, K), dtype=np.uint8) if a_fp8_init is None else np.array(a_fp8_init)
+    s = np.zeros((R, K // GROUP), dtype=np.uint8) if a_scale_init is None else np.array(a_scale_init)
+    for flat in range(R):
+        r = int(d2s[flat])
+        if 0 <= r < R:
+            a[r] = codes[flat // top_k]
+            s[r] = scales[flat // top_k]
     return a, s
 
 

@@ -41,6 +41,38 @@ def test_quantize_gather_bit_exact(cuda_lib, M, K, k, E, special):
     assert np.array_equal(a.cpu().numpy(), ra)
 
 
+@pytest.mark.parametrize("M,K,k,E,special", [(3, 128, 2, 4, False), (16, 512, 2, 4, True),
+                                             (64, 6144, 8, 32, True), (300, 2048, 8, 32, False),
+                                             (7, 8192, 1, 3, True)])
+def test_quantize_scatter_bit_exact(cuda_lib, M, K, k, E, special):
+    rng = np.random.default_rng(M * 11 + K)
+    x = _tokens(rng, M, K, special)
+    ids = make_routing(M, E, k, "biased", M + 2 * K)
+    _, s2d, d2s, _ = plan_expert_offsets(ids, E)
+    a, s = cuda_lib.hg_quantize_scatter_acts(x.cuda(), k, torch.from_numpy(d2s).cuda())
+    ga, gs = cuda_lib.hg_quantize_gather_acts(x.cuda(), k, torch.from_numpy(s2d).cuda())
+    torch.cuda.synchronize()
+    ra, rs = Q.quantize_scatter(x.view(torch.int16).numpy().view(np.uint16), k, d2s)
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(a.cpu().numpy(), ra)
+    assert torch.equal(a, ga) and torch.equal(s, gs)          # same codes as the gather
+
+
+def test_quantize_scatter_skips_dropped_and_out_of_range(cuda_lib):
+    rng = np.random.default_rng(10)
+    M, K, k = 8, 256, 2
+    x = _tokens(rng, M, K)
+    d2s = np.arange(M * k, dtype=np.int32)[::-1].copy()
+    d2s[[3, 9]] = -1
+    d2s[12] = M * k + 5                                      # outside the output: skipped
+    a = torch.full((M * k, K), 0xAB, dtype=torch.uint8, device="cuda")
+    s = torch.full((M * k, K // 128), 0xCD, dtype=torch.uint8, device="cuda")
+    cuda_lib.hg_quantize_scatter_acts(x.cuda(), k, torch.from_numpy(d2s).cuda(), a, s)
+    torch.cuda.synchronize()
+    ra, rs = Q.quantize_scatter(x.view(torch.int16).numpy().view(np.uint16), k, d2s,
+                                np.full((M * k, K), 0xAB, np.uint8), np.full((M * k, 2), 0xCD, np.uint8))
+    assert np.array_equal(a.cpu().numpy(), ra) and np.array_equal(s.cpu().numpy(), rs)
+
+
 def test_quantize_gather_skips_dropped_rows(cuda_lib):
     rng = np.random.default_rng(9)
     M, K, k = 8, 256, 2
@@ -86,7 +118,7 @@ def test_moe_layer_end_to_end(cuda_lib):
     w_fp4, w_scale = make_weights(E, N, K, seed=3)
     wts = rng.random((M, k)).astype(np.float32)
     off_t, s2d_t, d2s_t = cuda_lib.hg_plan_expert_offsets(torch.from_numpy(ids).cuda(), E)
-    a, s = cuda_lib.hg_quantize_gather_acts(x.cuda(), k, s2d_t)
+    a, s = cuda_lib.hg_quantize_scatter_acts(x.cuda(), k, d2s_t)
     y = cuda_lib.hg_grouped_w4a8_gemm(a, s, w_fp4.cuda(), w_scale.cuda(), off_t)
     out = cuda_lib.hg_combine_topk(y, d2s_t, torch.from_numpy(wts).cuda())
     torch.cuda.synchronize()

@@ -110,3 +110,27 @@ def test_combine_unpermutes_and_weights():
     d[3] = -1
     out2 = Q.combine_topk(yb, d, w)
     assert np.array_equal(out2[1], round_f64_to_bf16_bits(0.5 * yv[perm[2]]))
+
+
+def test_scatter_by_hand_and_equal_to_gather_on_a_plan():
+    x = np.arange(3 * 128, dtype=np.float32).reshape(3, 128) / 64
+    d2s = np.array([4, 1, -1, 0, 5, 9], dtype=np.int32)    # token 1 copy 0 dropped; 9 out of range
+    a, s = Q.quantize_scatter(_bf16_bits(x), 2, d2s, np.full((6, 128), 0xAB, np.uint8),
+                              np.full((6, 1), 0xCD, np.uint8))
+    codes, scales = Q.quantize_rows(_bf16_bits(x))
+    want = {4: 0, 1: 0, 0: 1, 5: 2}
+    for r in range(6):
+        if r in want:
+            assert np.array_equal(a[r], codes[want[r]]) and s[r, 0] == scales[want[r], 0]
+        else:
+            assert np.all(a[r] == 0xAB) and s[r, 0] == 0xCD
+    # on a plan's pair of permutations the scatter equals the gather
+    from oracle.plan import plan_expert_offsets
+    from synth import make_routing
+    rng = np.random.default_rng(8)
+    M, K, k, E = 40, 256, 4, 6
+    xb = _bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    _, s2d, d2s, _ = plan_expert_offsets(make_routing(M, E, k, "biased", 3), E)
+    ga, gs = Q.quantize_gather(xb, k, s2d)
+    sa, ss = Q.quantize_scatter(xb, k, d2s)
+    assert np.array_equal(ga, sa) and np.array_equal(gs, ss)
