@@ -191,41 +191,87 @@ quantize_scatter_kernel(const uint16_t* __restrict__ x, int M, int K, int top_k,
     }
 }
 
-// One warp per token: lanes 0..top_k-1 fetch the token's sorted rows and
-// weights, the warp shares them by shuffles, then every lane loads its 16
-// bytes of each of the top_k rows before accumulating (8 at a time).
+// Work item = (token, 2048-column slice), one warp each.  With top_k <= 32
+// lanes 0..top_k-1 fetch the token's sorted rows and weights once per item
+// and share them by shuffles; each lane then loads its 16 bytes of each of
+// the top_k rows for two 256-column chunks at a time (2 * top_k loads in
+// flight) before accumulating in FP32, j ascending.  Larger top_k take the
+// same steps in batches of 32 ids.
 constexpr int kCBatch = 8;
+constexpr int kCCols = 2048;
+
+__device__ __forceinline__ void combine_acc(float (&acc)[8], const uint4 v, float w) {
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(w, __uint_as_float(w4[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ uint4 combine_pack(const float (&acc)[8]) {
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]))) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1])))
+                << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 __global__ void combine_topk_kernel(const uint16_t* __restrict__ y,
                                     const int32_t* __restrict__ src_to_sorted,
                                     const float* __restrict__ weights, int M, int top_k, int N,
                                     uint16_t* __restrict__ out) {
     const int lane = threadIdx.x & 31;
-    const int warps = blockDim.x >> 5;
-    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < M; t += gridDim.x * warps) {
-        for (int n0 = 8 * lane; n0 < N; n0 += 256) {
-            float acc[8];
+    const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const int ncs = (N + kCCols - 1) / kCCols;
+    const long long items = static_cast<long long>(M) * ncs;
+    for (long long item = gw; item < items; item += nw) {
+        const int t = static_cast<int>(item / ncs);
+        const int cbeg = static_cast<int>(item % ncs) * kCCols;
+        const int cend = min(N, cbeg + kCCols);
+        const int32_t* rows_t = src_to_sorted + static_cast<long long>(t) * top_k;
+        const float* w_t = weights + static_cast<long long>(t) * top_k;
+        // the first 32 ids once per item (all of them when top_k <= 32)
+        int first_r = -1;
+        float first_w = 0.0f;
+        if (lane < top_k) {
+            first_r = __ldg(rows_t + lane);
+            first_w = __ldg(w_t + lane);
+        }
+        for (int n0 = cbeg + 8 * lane; n0 < cend; n0 += 512) {
+            const int n1 = n0 + 256;
+            const bool two = n1 < cend;
+            float acc0[8], acc1[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 8; ++i) acc0[i] = acc1[i] = 0.0f;
             for (int j0 = 0; j0 < top_k; j0 += 32) {
-                int my_r = -1;
-                float my_w = 0.0f;
-                if (j0 + lane < top_k) {
-                    my_r = __ldg(src_to_sorted + static_cast<long long>(t) * top_k + j0 + lane);
-                    my_w = __ldg(weights + static_cast<long long>(t) * top_k + j0 + lane);
+                int my_r = first_r;
+                float my_w = first_w;
+                if (j0 > 0) {
+                    my_r = -1;
+                    my_w = 0.0f;
+                    if (j0 + lane < top_k) {
+                        my_r = __ldg(rows_t + j0 + lane);
+                        my_w = __ldg(w_t + j0 + lane);
+                    }
                 }
                 const int nj = min(32, top_k - j0);
                 for (int b0 = 0; b0 < nj; b0 += kCBatch) {
-                    uint4 v[kCBatch];
+                    uint4 v0[kCBatch], v1[kCBatch];
                     float wj[kCBatch];
 #pragma unroll
                     for (int jj = 0; jj < kCBatch; ++jj) {
                         const int r = __shfl_sync(0xFFFFFFFFu, my_r, (b0 + jj) & 31);
                         wj[jj] = __shfl_sync(0xFFFFFFFFu, my_w, (b0 + jj) & 31);
-                        v[jj] = make_uint4(0, 0, 0, 0);
+                        v0[jj] = v1[jj] = make_uint4(0, 0, 0, 0);
                         if (b0 + jj < nj && r >= 0) {
-                            v[jj] = __ldg(reinterpret_cast<const uint4*>(
-                                y + static_cast<long long>(r) * N + n0));
+                            const uint16_t* yr = y + static_cast<long long>(r) * N;
+                            v0[jj] = __ldg(reinterpret_cast<const uint4*>(yr + n0));
+                            if (two) v1[jj] = __ldg(reinterpret_cast<const uint4*>(yr + n1));
                         } else {
                             wj[jj] = 0.0f;
                         }
@@ -233,25 +279,14 @@ __global__ void combine_topk_kernel(const uint16_t* __restrict__ y,
 #pragma unroll
                     for (int jj = 0; jj < kCBatch; ++jj) {
                         if (b0 + jj >= nj) break;
-                        const uint32_t w4[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            acc[2 * i] = fmaf(wj[jj], __uint_as_float(w4[i] << 16), acc[2 * i]);
-                            acc[2 * i + 1] =
-                                fmaf(wj[jj], __uint_as_float(w4[i] & 0xFFFF0000u), acc[2 * i + 1]);
-                        }
+                        combine_acc(acc0, v0[jj], wj[jj]);
+                        combine_acc(acc1, v1[jj], wj[jj]);
                     }
                 }
             }
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                o[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]))) |
-                       (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1])))
-                        << 16);
-            }
-            *reinterpret_cast<uint4*>(out + static_cast<long long>(t) * N + n0) =
-                make_uint4(o[0], o[1], o[2], o[3]);
+            uint16_t* ot = out + static_cast<long long>(t) * N;
+            *reinterpret_cast<uint4*>(ot + n0) = combine_pack(acc0);
+            if (two) *reinterpret_cast<uint4*>(ot + n1) = combine_pack(acc1);
         }
     }
 }
@@ -287,7 +322,8 @@ int quantize_scatter_max_top_k() { return kMaxScatterTopK; }
 cudaError_t launch_combine_topk(const uint16_t* y, const int32_t* d2s, const float* weights,
                                 int M, int top_k, int N, uint16_t* out, int num_sms,
                                 cudaStream_t stream) {
-    long long blocks = (M + 7) / 8;                   // 256 threads = 8 tokens per pass
+    const long long items = static_cast<long long>(M) * ((N + kCCols - 1) / kCCols);
+    long long blocks = (items + 7) / 8;              // 256 threads = 8 work items per pass
     const long long cap = static_cast<long long>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
