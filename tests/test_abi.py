@@ -94,6 +94,7 @@ def test_gemm_argument_validation(lib):
     assert _gemm(lib, N=200) == lib.HG_ERR_UNSUPPORTED_SHAPE
     assert _gemm(lib, K=384) == lib.HG_ERR_UNSUPPORTED_SHAPE
     assert _gemm(lib, E=5000) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, E=513) == lib.HG_ERR_UNSUPPORTED_SHAPE   # 512 experts at most
     assert _gemm(lib, w=0x4010) == lib.HG_ERR_INVALID_ARG      # W needs 32-byte alignment
     assert _gemm(lib, a=0x1008) == lib.HG_ERR_INVALID_ARG      # A needs 16-byte alignment
     assert _gemm(lib, ws=0x8001) == lib.HG_ERR_INVALID_ARG
@@ -109,3 +110,21 @@ def test_plan_argument_validation(lib):
     assert f(c(0x1000), 4, 8, 32, None, c(0x3000), c(0x4000), c(0x5000), 1 << 20, None) == lib.HG_ERR_INVALID_ARG
     assert f(c(0x1000), 4, 8, 32, c(0x2000), c(0x3000), c(0x4000), c(0x5000), 4, None) == lib.HG_ERR_INVALID_ARG
     assert f(None, 4, 8, 32, c(0x2000), c(0x3000), c(0x4000), c(0x5000), 1 << 20, None) == lib.HG_ERR_INVALID_ARG
+
+
+def test_quantize_scatter_argument_validation(lib):
+    c = ctypes.c_void_p
+    f = lib.lib.hg_quantize_scatter_acts
+    ok = dict(x=0x1000, M=4, K=256, k=2, d2s=0x2000, a=0x3000, s=0x4000)
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(c(a["x"]), a["M"], a["K"], a["k"], c(a["d2s"]), c(a["a"]), c(a["s"]), None)
+    assert call(M=-1) == lib.HG_ERR_INVALID_ARG
+    assert call(k=0) == lib.HG_ERR_INVALID_ARG
+    assert call(K=200) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert call(k=65) == lib.HG_ERR_UNSUPPORTED_SHAPE              # top_k <= 64
+    assert call(x=0) == lib.HG_ERR_INVALID_ARG
+    assert call(d2s=0) == lib.HG_ERR_INVALID_ARG
+    assert call(x=0x1008) == lib.HG_ERR_INVALID_ARG                # 16-byte alignment
+    assert call(a=0x3008) == lib.HG_ERR_INVALID_ARG
+    assert call(M=0, x=0, d2s=0, a=0, s=0) == lib.HG_OK            # empty: a no-op

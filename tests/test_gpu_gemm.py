@@ -116,6 +116,34 @@ def test_ragged_experts_random_codes(cuda_lib, variant, E, N, K, cuts):
     assert_rows_close(bf16_bits(out), ref, f"ragged E={E} N={N} K={K}")
 
 
+def test_max_experts_mostly_empty(cuda_lib, variant):
+    # 512 experts (the limit), most of them empty, a few with 1..40 rows
+    rng = np.random.default_rng(12)
+    E, N, K = 512, 128, 512
+    sizes = np.zeros(E, dtype=np.int64)
+    hot = rng.choice(E, 24, replace=False)
+    sizes[hot] = rng.integers(1, 41, 24)
+    cuts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(cuts[-1])
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    out = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K)
+    assert_rows_close(bf16_bits(out), ref, "E=512")
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+@pytest.mark.parametrize("E,cuts", [(1, [0, 1]), (2, [0, 0, 1]), (1, [0, 17])])
+def test_minimum_shapes(cuda_lib, variant, E, cuts):
+    # N = 128 (one weight tile), K = 512 (the smallest supported), one or a few rows
+    rng = np.random.default_rng(13 + len(cuts) + cuts[-1])
+    N, K = 128, 512
+    R = cuts[-1]
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    out = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K)
+    assert_rows_close(bf16_bits(out), ref, f"minimum E={E} rows={R}")
+
+
 def test_wide_scale_range(cuda_lib, variant):
     rng = np.random.default_rng(5)
     E, N, K, R = 2, 256, 1024, 70
