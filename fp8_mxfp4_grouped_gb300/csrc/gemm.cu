@@ -65,8 +65,9 @@ struct GemmCfg {
     static constexpr uint32_t kRxSlotBytes = 32 * T * 4;     // one lane quadrant, FP32
     static constexpr int kRxSlots = CL == 1 ? 0 : (CL == 2 ? 2 : 3);
     static constexpr uint32_t kRxBytes = kRxSlots * kRxSlotBytes;
-    static constexpr int kSfWarps = S;                     // one scale warp per ring slot
-    static constexpr int kThreads = 32 * (6 + S);          // TMA, MMA, 4 epilogue, S scale warps
+    // scale warps take the stages in turn: one per ring slot, at most four
+    static constexpr int kSfWarps = S < 4 ? S : 4;
+    static constexpr int kThreads = 32 * (6 + kSfWarps);   // TMA, MMA, 4 epilogue, scale warps
     static constexpr uint32_t kATileBytes = T * kBK;
     static constexpr int kSfbAtoms = T > 128 ? 2 : 1;      // 128 tokens per scale block
     static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
@@ -99,7 +100,7 @@ struct GemmCfg {
     static_assert(kSfCol0 + S * kSfSlotCols <= kTmemCols, "TMEM budget");
     static_assert(kMaxExperts >= 32 && smem_bytes(kMaxExperts) <= kSmemBudget,
                   "shared memory budget");
-    static_assert(C * 32 * (6 + S) * 96 <= 65536, "registers for C resident CTAs");
+    static_assert(C * kThreads * 96 <= 65536, "registers for C resident CTAs");
 };
 
 // CTA-pair shape (tcgen05 cta_group::2).  T: largest token tile (MMA N,
