@@ -382,7 +382,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_w = ptx::policy_evict_last();   // weight tiles are re-read by the other token tiles of their expert
             const uint64_t pol_a = ptx::policy_evict_last();
             uint32_t g = 0;
             bool ok = true;
@@ -802,7 +802,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_w = ptx::policy_evict_last();   // weight tiles are re-read by the other token tiles of their expert
             const uint64_t pol_a = ptx::policy_evict_last();
             const uint32_t full_tma_leader = ptx::mapa_shared(bar_full_tma, 0);
             uint32_t g = 0;
