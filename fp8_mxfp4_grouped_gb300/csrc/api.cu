@@ -38,6 +38,7 @@ int choose_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms) {
     if (!v) v = gemm_pick_variant(E, N, K, rows, num_sms);
     if (v == 4 && N % 256 != 0) v = 3;   // CTA pairs split 256 weight rows
     if (v == 5 && N % 256 != 0) v = 2;
+    if (v == 7 && N % 256 != 0) v = 2;   // two 128-row weight blocks per unit
     return v;
 }
 
@@ -382,7 +383,7 @@ int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows) {
 }
 
 int32_t hg_set_gemm_variant(int32_t variant) {
-    if (variant < 0 || variant > 6) return -1;
+    if (variant < 0 || variant > 7) return -1;
     return g_forced_variant.exchange(variant);
 }
 

@@ -54,12 +54,16 @@ constexpr uint32_t kSmemReservedPerBlock = 1024;
 // K loop of every unit over 2 or CL of them (split-K, chosen on the device
 // from the unit count); each CTA then holds receive slots for the FP32
 // partial tiles of the others.
-template <int T, int S, int C, int CL = 1>
+// MB: 128-row weight blocks per unit.  With MB = 2 a unit covers 256 weight
+// rows as two M = 128 MMAs per K step that share the stage's token tile (one
+// activation tile per two weight tiles, two accumulators).
+template <int T, int S, int C, int CL = 1, int MB = 1>
 struct GemmCfg {
     static constexpr int kTMax = T;
     static constexpr int kStages = S;
     static constexpr int kCtasPerSm = C;
     static constexpr int kCluster = CL;
+    static constexpr int kMB = MB;
     // A CTA of a split group finalises 4/s of the four TMEM lane quadrants
     // and receives s-1 partials of each: (4/s)(s-1) slots, at most 3.
     static constexpr uint32_t kRxSlotBytes = 32 * T * 4;     // one lane quadrant, FP32
@@ -71,14 +75,14 @@ struct GemmCfg {
     static constexpr uint32_t kATileBytes = T * kBK;
     static constexpr int kSfbAtoms = T > 128 ? 2 : 1;      // 128 tokens per scale block
     static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
-    static constexpr uint32_t kAccCols = T;                // TMEM columns per accumulator
+    static constexpr uint32_t kAccCols = MB * T;           // TMEM columns per accumulator buffer
     static constexpr uint32_t kTmemCols = 512 / C;
-    static constexpr uint32_t kSfCol0 = 2 * kAccCols;      // scale slots after both accumulators
-    static constexpr uint32_t kSfSlotCols = 4 + 4 * kSfbAtoms;
-    static constexpr uint32_t kOffW = 0;
-    static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
+    static constexpr uint32_t kSfCol0 = 2 * kAccCols;      // scale slots after both buffers
+    static constexpr uint32_t kSfSlotCols = 4 * MB + 4 * kSfbAtoms;
+    static constexpr uint32_t kOffW = 0;                   // [stage][block] weight tiles
+    static constexpr uint32_t kOffA = kOffW + S * MB * kWTileBytes;
     static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
-    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;
+    static constexpr uint32_t kOffSfb = kOffSfa + S * MB * kSfaBytes;
     static constexpr uint32_t kOffRx = kOffSfb + S * kSfbBytes;
     static constexpr uint32_t kOffBar = kOffRx + kRxBytes;
     static constexpr uint32_t kOffMisc = kOffBar + 256;
@@ -89,6 +93,7 @@ struct GemmCfg {
     static constexpr size_t kSmemBudget =
         C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
     static_assert(CL == 1 || CL == 2 || CL == 4, "split over 2 or 4 CTAs");
+    static_assert(MB == 1 || (MB == 2 && CL == 1), "two weight blocks per unit, without split-K");
     static_assert(8 * (3 * S + 5 + 8) <= 256, "barrier area");
     // experts whose scheduler tables still fit next to the ring (<= kMaxE)
     static constexpr int kMaxExperts =
@@ -149,6 +154,7 @@ using CfgSmall = GemmCfg<64, 4, 2>;    // few rows per expert: HBM-bound weight 
 using CfgMid = GemmCfg<112, 3, 2>;     // a few hundred rows per expert
 using CfgLarge = GemmCfg<224, 4, 1>;   // many rows per expert: tensor-bound
 using CfgSplit = GemmCfg<32, 4, 2, 4>; // few units per CTA: split-K over clusters of 4
+using CfgDual = GemmCfg<112, 4, 1, 1, 2>;   // 256 weight rows per unit, one token tile shared
 
 // Split-K factor for a launch of G CTAs (a multiple of max_split) over U
 // units of KT stages: the s in {1, 2, 4} that minimises the stages of the
@@ -174,7 +180,8 @@ struct Sched {
     const int32_t* tile;
     const int32_t* prefix;   // [E+1] exclusive prefix of units per expert
     int E;
-    int NT;                  // weight-row tiles per expert (N / 128)
+    int NT;                  // weight-row tiles per expert (N / (128 * blocks per unit))
+    int wstep;               // weight rows per unit (128 * blocks per unit)
 };
 
 struct Unit {
@@ -198,7 +205,7 @@ __device__ __forceinline__ Unit decode_unit(const Sched& s, int u) {
     const int nt = local / ntt;
     const int tt = local - nt * ntt;
     const int tile = s.tile[lo];
-    t.n0 = nt * kBW;
+    t.n0 = nt * s.wstep;
     t.row0 = s.start[lo] + tt * tile;
     t.nrows = min(tile, s.rows[lo] - tt * tile);
     t.n_mma = (t.nrows + 15) & ~15;
@@ -314,7 +321,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     }
 
     // Per-expert token tiling, from the expert's own row count.
-    const int NT = N / kBW;
+    const int NT = N / (kBW * Cfg::kMB);
     for (int e = threadIdx.x; e < E; e += Cfg::kThreads) {
         const int lo = offsets[e];
         const int hi = offsets[e + 1];
@@ -359,7 +366,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     ptx::tc_fence_after();
 
     const uint32_t tmem_base = misc[0];
-    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT};
+    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT, kBW * Cfg::kMB};
     const int U = s_prefix[E];
     const int KT = K / kBK;
     const WaitCtx wctx{status, misc + 1, timeout_ns};
@@ -398,9 +405,12 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                         break;
                     }
                     const uint32_t fb = bar_full_tma + 8 * slot;
-                    ptx::mbar_arrive_expect_tx(fb, kWTileTx + t.n_mma * kBK);
-                    ptx::tma_load_2d(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w, ks * kBK,
-                                     wrow, fb, pol_w);
+                    ptx::mbar_arrive_expect_tx(fb, Cfg::kMB * kWTileTx + t.n_mma * kBK);
+#pragma unroll
+                    for (int mb = 0; mb < Cfg::kMB; ++mb) {
+                        ptx::tma_load_2d(sbase + Cfg::kOffW + (slot * Cfg::kMB + mb) * kWTileBytes,
+                                         &map_w, ks * kBK, wrow + mb * kBW, fb, pol_w);
+                    }
                     load_a_rows(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes, ks * kBK,
                                 t.row0, t.n_mma, fb, pol_a);
                 }
@@ -438,22 +448,33 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                         break;
                     }
                     ptx::tc_fence_after();
+                    // scale slot: [weight block 0..MB-1: 4 cols each][token atoms: 4 cols each]
                     const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
-                    const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
+                    const uint32_t sfb_col = sf_col + 4 * Cfg::kMB;
+                    const uint32_t sfa = sbase + Cfg::kOffSfa + slot * Cfg::kMB * kSfaBytes;
                     const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
-                    ptx::tc_cp_32x128b_warpx4(sf_col, ptx::desc_sf_32x16(sfa));
-                    ptx::tc_cp_32x128b_warpx4(sf_col + 4, ptx::desc_sf_32x16(sfb));
-                    if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
-                        ptx::tc_cp_32x128b_warpx4(sf_col + 8, ptx::desc_sf_32x16(sfb + 512));
+#pragma unroll
+                    for (int mb = 0; mb < Cfg::kMB; ++mb) {
+                        ptx::tc_cp_32x128b_warpx4(sf_col + 4 * mb,
+                                                  ptx::desc_sf_32x16(sfa + mb * kSfaBytes));
                     }
-                    const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
+                    ptx::tc_cp_32x128b_warpx4(sfb_col, ptx::desc_sf_32x16(sfb));
+                    if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
+                        ptx::tc_cp_32x128b_warpx4(sfb_col + 4, ptx::desc_sf_32x16(sfb + 512));
+                    }
+                    const uint32_t wsm = sbase + Cfg::kOffW + slot * Cfg::kMB * kWTileBytes;
                     const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk) {
-                        ptx::mma_mxf8f6f4_1x(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
-                                             ptx::desc_kmajor_sw128(asm_ + kk * 32),
-                                             ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
-                                             sf_col + 4, (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
+#pragma unroll
+                        for (int mb = 0; mb < Cfg::kMB; ++mb) {
+                            ptx::mma_mxf8f6f4_1x(
+                                d_tmem + mb * kTMax,
+                                ptx::desc_kmajor_sw128(wsm + mb * kWTileBytes + kk * 32),
+                                ptx::desc_kmajor_sw128(asm_ + kk * 32),
+                                ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col + 4 * mb, sfb_col,
+                                (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
+                        }
                     }
                     ptx::tc_commit(bar_empty + 8 * slot);
                 }
@@ -489,17 +510,20 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
             if constexpr (kCL == 1) {
-                const int n = t.n0 + 32 * q + lane;
-                uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
-                for (int c0 = 0; c0 < t.nrows; c0 += 16) {
-                    uint32_t v[16];
-                    ptx::tmem_ld_32x32b_x16(taddr + c0, v);
-                    ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        if (c0 + j < t.nrows) {
-                            dst[static_cast<size_t>(c0 + j) * N] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                for (int mb = 0; mb < Cfg::kMB; ++mb) {
+                    const int n = t.n0 + mb * kBW + 32 * q + lane;
+                    uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
+                    for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+                        uint32_t v[16];
+                        ptx::tmem_ld_32x32b_x16(taddr + mb * kTMax + c0, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (c0 + j < t.nrows) {
+                                dst[static_cast<size_t>(c0 + j) * N] = __bfloat16_as_ushort(
+                                    __float2bfloat16_rn(__uint_as_float(v[j])));
+                            }
                         }
                     }
                 }
@@ -610,10 +634,14 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 const uint32_t ph = (g / kStages) & 1u;
                 // Weight scales: row n = lane + 32c, the four 32-K blocks of
                 // this stage in one 32-bit word (byte i = block i).
-                uint32_t wv[4];
+                uint32_t wv[Cfg::kMB][4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    wv[c] = ldg_u32(wsrc + static_cast<size_t>(32 * c) * ws_row + ks * 4);
+                for (int mb = 0; mb < Cfg::kMB; ++mb) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        wv[mb][c] = ldg_u32(wsrc + static_cast<size_t>(mb * kBW + 32 * c) * ws_row +
+                                            ks * 4);
+                    }
                 }
                 // Token scales: one per 128-K group, replicated into the four
                 // 32-K blocks.  Token index = 128a + lane + 32c.
@@ -634,9 +662,13 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     ok = false;
                     break;
                 }
-                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes + 16 * lane;
+                const uint32_t sfa =
+                    sbase + Cfg::kOffSfa + slot * Cfg::kMB * kSfaBytes + 16 * lane;
                 const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes + 16 * lane;
-                sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
+#pragma unroll
+                for (int mb = 0; mb < Cfg::kMB; ++mb) {
+                    sts_v4(sfa + mb * kSfaBytes, wv[mb][0], wv[mb][1], wv[mb][2], wv[mb][3]);
+                }
                 sts_v4(sfb, av[0], av[1], av[2], av[3]);
                 if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
                     sts_v4(sfb + 512, av[4 % (4 * Cfg::kSfbAtoms)], av[5 % (4 * Cfg::kSfbAtoms)],
@@ -772,7 +804,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     ptx::tc_fence_after();
 
     const uint32_t tmem_base = misc[0];
-    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT};
+    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT, 2 * kBW};
     const int U = s_prefix[E];
     const int KT = K / kBK;
     const WaitCtx wctx{status, misc + 1, timeout_ns};
@@ -1097,7 +1129,7 @@ cudaError_t set_smem_attr(Kern* fn, size_t bytes) {
 template <class Cfg>
 long long grid_plain(const GemmArgs& a) {
     long long grid = static_cast<long long>(a.num_sms) * Cfg::kCtasPerSm;
-    const long long u = units_upper(a, Cfg::kTMax, kBW);
+    const long long u = units_upper(a, Cfg::kTMax, kBW * Cfg::kMB);
     return u < grid ? u : grid;
 }
 
@@ -1190,6 +1222,7 @@ int gemm_variant_max_experts(int variant) {
         case 2: return CfgMid::kMaxExperts;
         case 3: return CfgLarge::kMaxExperts;
         case 6: return CfgSplit::kMaxExperts;
+        case 7: return CfgDual::kMaxExperts;
         default: return kMaxE;
     }
 }
@@ -1238,6 +1271,7 @@ int gemm_variant_token_tile(int variant) {
         case 4: return CfgPair::kTMax;
         case 5: return CfgPairMid::kTMax;
         case 6: return CfgSplit::kTMax;
+        case 7: return CfgDual::kTMax;
         default: return 0;
     }
 }
@@ -1249,6 +1283,7 @@ size_t gemm_smem_bytes(int variant, int32_t E) {
         case 4: return CfgPair::smem_bytes(E);
         case 5: return CfgPairMid::smem_bytes(E);
         case 6: return CfgSplit::smem_bytes(E);
+        case 7: return CfgDual::smem_bytes(E);
         default: return CfgLarge::smem_bytes(E);
     }
 }
@@ -1260,6 +1295,7 @@ long long gemm_launch_ctas(const GemmArgs& a) {
         case 4: return grid_pair<CfgPair>(a);
         case 5: return grid_pair<CfgPairMid>(a);
         case 6: return grid_cluster<CfgSplit>(a);
+        case 7: return grid_plain<CfgDual>(a);
         default: return grid_plain<CfgLarge>(a);
     }
 }
@@ -1272,6 +1308,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, con
         case 4: return launch_pair<CfgPair>(a, map_w, map_a, stream);
         case 5: return launch_pair<CfgPairMid>(a, map_w, map_a, stream);
         case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, stream);
+        case 7: return launch_cfg<CfgDual>(a, map_w, map_a, stream);
         default: return launch_cfg<CfgLarge>(a, map_w, map_a, stream);
     }
 }

@@ -20,8 +20,8 @@ T_MAX depends on the pipeline variant the library picks from rows / E
 from __future__ import annotations
 
 T_MAX = 224
-VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96, 6: 32}
-VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32, 6: 16}   # CTA pairs split the token tile in two
+VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96, 6: 32, 7: 112}
+VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32, 6: 16, 7: 16}   # CTA pairs split the token tile in two
 SPLIT_CLUSTER = 4        # variant 6: clusters of 4 CTAs, two per SM
 MMA_N_STEP = 16
 W_TILE = 128

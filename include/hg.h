@@ -206,7 +206,9 @@ int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows);
  * CTAs per SM in clusters of four that split the K loop of each tile over 1,
  * 2 or 4 CTAs (chosen on the device to even out the work when there are few
  * tiles per CTA; the partial sums are added in a fixed order, so results do
- * not vary from run to run).  Meant for tests and tuning.  Returns the
+ * not vary from run to run), 7 = 112-row tiles with one CTA per SM and 256
+ * weight rows per tile (two 128-row MMAs sharing each token tile; N % 256 ==
+ * 0, else variant 2).  Meant for tests and tuning.  Returns the
  * previous setting, or -1 for an invalid value (setting unchanged).
  * Host-only.
  */

@@ -49,10 +49,13 @@ def test_variant_choice_mirrors_the_library():
         hg.hg_set_gemm_variant(5)
         assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 96
         assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 112   # falls back to variant 2
+        hg.hg_set_gemm_variant(7)
+        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 112
+        assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 112   # falls back to variant 2
     finally:
         hg.hg_set_gemm_variant(prev)
     with pytest.raises(ValueError):
-        hg.hg_set_gemm_variant(7)
+        hg.hg_set_gemm_variant(8)
 
 
 def test_tile_inflation_vs_fixed_128():
