@@ -13,16 +13,22 @@
 //    multiple of 16 up to 256, so each expert's token tile is sized from its
 //    own row count at instruction granularity: an expert with 130 rows gets
 //    one 144-token tile, not two 128-row tiles.
-//  * one persistent CTA per SM walks a unit list (expert, weight-row tile,
-//    token tile) built on the device from expert_offsets; no host sync.
-//  * warp roles: warp 0 issues TMA loads (weights through the 16U4_ALIGN16B
-//    unpacking TMA type, activations as bytes; no multicast) and L2
-//    prefetches several stages ahead; warps 2,3,8,9,10 stage the block scales into the tensor core's scale layout (activation
-//    scales are per 128-K, replicated into the four 32-K blocks they cover);
-//    warp 1 copies scales to TMEM and issues tcgen05.mma kind::mxf8f6f4 with
-//    block scaling, accumulating FP32 in TMEM; warps 4..7 drain the TMEM
-//    accumulator (double-buffered) to BF16 with stores cut at the expert's
-//    last row.
+//  * persistent CTAs (one or two per SM, sized to one wave) walk a unit list
+//    (expert, weight-row tile, token tile) built on the device from
+//    expert_offsets; no host sync.
+//  * warp roles: warp 0 issues the TMA loads (weights through the
+//    16U4_ALIGN16B unpacking TMA type, activations as bytes in boxes of
+//    128/64/32/16 rows; both with the L2 evict-last hint; no multicast);
+//    up to four scale warps (2, 3, 8, 9) stage the block scales into the
+//    tensor core's scale layout (activation scales are per 128-K, replicated
+//    into the four 32-K blocks they cover); warp 1 copies scales to TMEM and
+//    issues tcgen05.mma kind::mxf8f6f4 with block scaling, accumulating FP32
+//    in TMEM; warps 4..7 drain the TMEM accumulator (double-buffered) to BF16
+//    with stores cut at the expert's last row.
+//  * variants (GemmCfg): token tile, ring depth, CTAs per SM; split-K over
+//    clusters of four (partials reduce-scattered through distributed shared
+//    memory); two 128-row weight blocks per unit; and a CTA-pair kernel
+//    (tcgen05 cta_group::2, grouped_w4a8_pair_kernel).
 //  * every barrier wait is bounded (see wait_bounded).
 #include <cuda_bf16.h>
 

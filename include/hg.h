@@ -156,9 +156,12 @@ hg_status hg_plan_expert_offsets_noalloc(const int32_t* topk_ids, int32_t M, int
  * are skipped and HG_ERR_BAD_OFFSETS is recorded for hg_get_device_status.
  * E2M1/E4M3 NaN codes and E8M0 code 255 are not supported inputs.
  * One persistent kernel launch on `stream`; no host synchronisation.  The
- * pipeline shape (largest token tile, CTAs per SM) is chosen from the mean
- * rows per expert, rows / E; results do not depend on the choice beyond the
- * FP32 summation order inside one output element, which is the same for all.
+ * pipeline shape (largest token tile, CTAs per SM, split-K) is chosen from
+ * the mean rows per expert, rows / E, and for launches with few weight tiles
+ * per CTA from the device's resident CTA count.  Shapes differ only in FP32
+ * rounding (the split-K shape sums the partial products of K ranges in K
+ * order); for given arguments on a given device the result is the same on
+ * every run.
  */
 hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
                                const uint8_t* w_fp4, const uint8_t* w_scale,
