@@ -383,7 +383,7 @@ int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows) {
 }
 
 int32_t hg_set_gemm_variant(int32_t variant) {
-    if (variant < 0 || variant > 7) return -1;
+    if (variant < 0 || variant > 8) return -1;
     return g_forced_variant.exchange(variant);
 }
 

@@ -63,13 +63,17 @@ constexpr uint32_t kSmemReservedPerBlock = 1024;
 // MB: 128-row weight blocks per unit.  With MB = 2 a unit covers 256 weight
 // rows as two M = 128 MMAs per K step that share the stage's token tile (one
 // activation tile per two weight tiles, two accumulators).
-template <int T, int S, int C, int CL = 1, int MB = 1>
+// AB: TMEM accumulator buffers.  With AB = 1 the MMAs of the next unit wait
+// for the epilogue to drain the accumulator (the other CTA on the SM keeps the
+// tensor core busy meanwhile); it lets a 224-row token tile run two CTAs per SM.
+template <int T, int S, int C, int CL = 1, int MB = 1, int AB = 2>
 struct GemmCfg {
     static constexpr int kTMax = T;
     static constexpr int kStages = S;
     static constexpr int kCtasPerSm = C;
     static constexpr int kCluster = CL;
     static constexpr int kMB = MB;
+    static constexpr int kAccBufs = AB;
     // A CTA of a split group finalises 4/s of the four TMEM lane quadrants
     // and receives s-1 partials of each: (4/s)(s-1) slots, at most 3.
     static constexpr uint32_t kRxSlotBytes = 32 * T * 4;     // one lane quadrant, FP32
@@ -83,7 +87,7 @@ struct GemmCfg {
     static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
     static constexpr uint32_t kAccCols = MB * T;           // TMEM columns per accumulator buffer
     static constexpr uint32_t kTmemCols = 512 / C;
-    static constexpr uint32_t kSfCol0 = 2 * kAccCols;      // scale slots after both buffers
+    static constexpr uint32_t kSfCol0 = AB * kAccCols;     // scale slots after the buffers
     static constexpr uint32_t kSfSlotCols = 4 * MB + 4 * kSfbAtoms;
     static constexpr uint32_t kOffW = 0;                   // [stage][block] weight tiles
     static constexpr uint32_t kOffA = kOffW + S * MB * kWTileBytes;
@@ -100,6 +104,7 @@ struct GemmCfg {
         C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
     static_assert(CL == 1 || CL == 2 || CL == 4, "split over 2 or 4 CTAs");
     static_assert(MB == 1 || (MB == 2 && CL == 1), "two weight blocks per unit, without split-K");
+    static_assert(AB == 2 || (AB == 1 && CL == 1), "one accumulator buffer, without split-K");
     static_assert(8 * (3 * S + 5 + 8) <= 256, "barrier area");
     // experts whose scheduler tables still fit next to the ring (<= kMaxE)
     static constexpr int kMaxExperts =
@@ -161,6 +166,7 @@ using CfgMid = GemmCfg<112, 3, 2>;     // a few hundred rows per expert
 using CfgLarge = GemmCfg<224, 4, 1>;   // many rows per expert: tensor-bound
 using CfgSplit = GemmCfg<32, 4, 2, 4>; // few units per CTA: split-K over clusters of 4
 using CfgDual = GemmCfg<112, 4, 1, 1, 2>;   // 256 weight rows per unit, one token tile shared
+using CfgWide2 = GemmCfg<224, 2, 2, 1, 1, 1>;   // 224-row tiles, two CTAs per SM, one TMEM buffer each
 
 // Split-K factor for a launch of G CTAs (a multiple of max_split) over U
 // units of KT stages: the s in {1, 2, 4} that minimises the stages of the
@@ -436,8 +442,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
                  u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x), ++tc) {
                 const Unit t = decode_unit(sch, u);
-                const uint32_t b = tc & 1u;
-                if (!wait_bounded(bar_tempty + 8 * b, ((tc >> 1) & 1u) ^ 1u, wctx, kRoleMma,
+                const uint32_t b = tc % Cfg::kAccBufs;
+                if (!wait_bounded(bar_tempty + 8 * b, ((tc / Cfg::kAccBufs) & 1u) ^ 1u, wctx, kRoleMma,
                                   0x100u | b)) {
                     break;
                 }
@@ -510,8 +516,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); u < U;
              u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x), ++tc) {
             const Unit t = decode_unit(sch, u);
-            const uint32_t b = tc & 1u;
-            if (!wait_bounded(bar_tfull + 8 * b, (tc >> 1) & 1u, wctx, kRoleEpilogue, b)) break;
+            const uint32_t b = tc % Cfg::kAccBufs;
+            if (!wait_bounded(bar_tfull + 8 * b, (tc / Cfg::kAccBufs) & 1u, wctx, kRoleEpilogue, b)) break;
             ptx::tc_fence_after();
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
@@ -1229,13 +1235,16 @@ int gemm_variant_max_experts(int variant) {
         case 3: return CfgLarge::kMaxExperts;
         case 6: return CfgSplit::kMaxExperts;
         case 7: return CfgDual::kMaxExperts;
+        case 8: return CfgWide2::kMaxExperts;
         default: return kMaxE;
     }
 }
 
 // Variant choice from the mean rows per expert (the per-expert counts live on
 // the device).  Few rows: weight streaming dominates and two small pipelines
-// per SM keep the MMA issue rate up; many rows: the widest token tile.  With
+// per SM keep the MMA issue rate up; many rows: the widest token tile, two
+// CTAs per SM with one TMEM accumulator each (measured faster than one CTA
+// per SM with two accumulators above ~200 rows per expert).  With
 // at most 32 rows per expert the split-K variant is taken when, counting one
 // token tile per active expert (at most min(E, rows) of them), it leaves the
 // busiest CTA at least 15 % fewer stages than variant 1 (num_sms = 0: no
@@ -1265,8 +1274,8 @@ int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms
         }
         return 1;
     }
-    if (per <= 640) return 2;
-    return 3;
+    if (per <= 192) return 2;
+    return 8;
 }
 
 int gemm_variant_token_tile(int variant) {
@@ -1278,6 +1287,7 @@ int gemm_variant_token_tile(int variant) {
         case 5: return CfgPairMid::kTMax;
         case 6: return CfgSplit::kTMax;
         case 7: return CfgDual::kTMax;
+        case 8: return CfgWide2::kTMax;
         default: return 0;
     }
 }
@@ -1290,6 +1300,7 @@ size_t gemm_smem_bytes(int variant, int32_t E) {
         case 5: return CfgPairMid::smem_bytes(E);
         case 6: return CfgSplit::smem_bytes(E);
         case 7: return CfgDual::smem_bytes(E);
+        case 8: return CfgWide2::smem_bytes(E);
         default: return CfgLarge::smem_bytes(E);
     }
 }
@@ -1302,6 +1313,7 @@ long long gemm_launch_ctas(const GemmArgs& a) {
         case 5: return grid_pair<CfgPairMid>(a);
         case 6: return grid_cluster<CfgSplit>(a);
         case 7: return grid_plain<CfgDual>(a);
+        case 8: return grid_plain<CfgWide2>(a);
         default: return grid_plain<CfgLarge>(a);
     }
 }
@@ -1315,6 +1327,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, con
         case 5: return launch_pair<CfgPairMid>(a, map_w, map_a, stream);
         case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, stream);
         case 7: return launch_cfg<CfgDual>(a, map_w, map_a, stream);
+        case 8: return launch_cfg<CfgWide2>(a, map_w, map_a, stream);
         default: return launch_cfg<CfgLarge>(a, map_w, map_a, stream);
     }
 }

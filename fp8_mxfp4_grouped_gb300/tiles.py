@@ -14,14 +14,14 @@ tcgen05 kernel where an expert's tokens are the MMA's N side:
     the last tile of an expert issues MMA N = round_up_16(rows left)
 
 T_MAX depends on the pipeline variant the library picks from rows / E
-(``hg_gemm_token_tile``): 64, 112 or 224.  With T_MAX = 224 an expert with
+(``hg_gemm_token_tile``): 64, 112 or 224 (32 for split-K).  With T_MAX = 224 an expert with
 130 rows takes one 144-column tile where a fixed 128-row tile would take two.
 """
 from __future__ import annotations
 
 T_MAX = 224
-VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96, 6: 32, 7: 112}
-VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32, 6: 16, 7: 16}   # CTA pairs split the token tile in two
+VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96, 6: 32, 7: 112, 8: 224}
+VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32, 6: 16, 7: 16, 8: 16}   # CTA pairs split the token tile in two
 SPLIT_CLUSTER = 4        # variant 6: clusters of 4 CTAs, two per SM
 MMA_N_STEP = 16
 W_TILE = 128
@@ -48,9 +48,9 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
                 if 20 * c6 <= 17 * c1:
                     return 6
         return 1
-    if per <= 640:
+    if per <= 192:
         return 2
-    return 3
+    return 8
 
 
 def expert_tiling(rows_e: int, t_max: int = T_MAX, step: int = MMA_N_STEP):

@@ -211,7 +211,8 @@ int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows);
  * tiles per CTA; the partial sums are added in a fixed order, so results do
  * not vary from run to run), 7 = 112-row tiles with one CTA per SM and 256
  * weight rows per tile (two 128-row MMAs sharing each token tile; N % 256 ==
- * 0, else variant 2).  Meant for tests and tuning.  Returns the
+ * 0, else variant 2), 8 = 224-row tiles with two CTAs per SM and one TMEM
+ * accumulator each.  Meant for tests and tuning.  Returns the
  * previous setting, or -1 for an invalid value (setting unchanged).
  * Host-only.
  */

@@ -17,7 +17,7 @@ from tests.gpu_util import assert_rows_close, bf16_bits, np_u8
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [1, 2, 3, 4, 5, 6, 7]   # see hg_set_gemm_variant
+VARIANTS = [1, 2, 3, 4, 5, 6, 7, 8]   # see hg_set_gemm_variant
 
 
 @pytest.fixture(params=VARIANTS, ids=lambda v: f"variant{v}")

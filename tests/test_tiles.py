@@ -37,7 +37,7 @@ def test_variant_choice_mirrors_the_library():
     from fp8_mxfp4_grouped_gb300 import hg
     for E in (1, 4, 12, 32, 100, 512):
         for N in (256, 3584, 4096, 6144):
-            for rows in (0, 1, 16, 48 * E, 48 * E + E, 640 * E, 640 * E + E, 131072):
+            for rows in (0, 1, 16, 48 * E, 48 * E + E, 192 * E, 192 * E + E, 640 * E, 131072):
                 v = T.pick_variant(E, N, rows)
                 assert hg.hg_gemm_token_tile(E, N, 6144, rows) == T.VARIANT_T_MAX[v], (E, N, rows)
     prev = hg.hg_set_gemm_variant(2)
@@ -55,7 +55,7 @@ def test_variant_choice_mirrors_the_library():
     finally:
         hg.hg_set_gemm_variant(prev)
     with pytest.raises(ValueError):
-        hg.hg_set_gemm_variant(8)
+        hg.hg_set_gemm_variant(9)
 
 
 def test_tile_inflation_vs_fixed_128():
