@@ -1244,7 +1244,8 @@ int gemm_variant_max_experts(int variant) {
 // the device).  Few rows: weight streaming dominates and two small pipelines
 // per SM keep the MMA issue rate up; many rows: the widest token tile, two
 // CTAs per SM with one TMEM accumulator each (measured faster than one CTA
-// per SM with two accumulators above ~200 rows per expert).  With
+// per SM with two accumulators above ~200 rows per expert), with a wave
+// model moving the boundary when the device is known.  With
 // at most 32 rows per expert the split-K variant is taken when, counting one
 // token tile per active expert (at most min(E, rows) of them), it leaves the
 // busiest CTA at least 15 % fewer stages than variant 1 (num_sms = 0: no
@@ -1274,8 +1275,24 @@ int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms
         }
         return 1;
     }
-    if (per <= 192) return 2;
-    return 8;
+    // Above 48 rows per expert: variant 2 (112-row tiles, two accumulators)
+    // or variant 8 (224-row tiles, one accumulator), both two CTAs per SM.
+    // Wave model with every expert at the mean: rounds = units / resident
+    // CTAs rounded up; a variant-8 round costs 1.25 + 0.0026 * tile rows
+    // variant-2 rounds (measured at 112-224 rows per expert).  Skewed
+    // routing leaves more partial tiles than the model counts, so the model
+    // only moves the 192-row default when it predicts a 15 % gain.
+    const int def = per <= 192 ? 2 : 8;
+    if (num_sms <= 0 || N < kBW) return def;
+    const long long g = 2LL * num_sms;
+    const long long blocks = static_cast<long long>(E) * (N / kBW);
+    const long long t2 = (per + CfgMid::kTMax - 1) / CfgMid::kTMax;
+    const long long t8 = (per + CfgWide2::kTMax - 1) / CfgWide2::kTMax;
+    const long long rows8 = ((per + t8 - 1) / t8 + 15) / 16 * 16;
+    const long long c2 = (blocks * t2 + g - 1) / g * 10000;
+    const long long c8 = (blocks * t8 + g - 1) / g * (12500 + 26 * rows8);
+    if (def == 2) return 100 * c8 <= 85 * c2 ? 8 : 2;
+    return 100 * c8 >= 118 * c2 ? 2 : 8;
 }
 
 int gemm_variant_token_tile(int variant) {

@@ -34,7 +34,9 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     With a device (num_sms > 0, split_ctas = the split-K variant's resident
     CTAs) and at most 32 rows per expert, variant 6 is taken when, counting
     one token tile per active expert, it leaves the busiest CTA at least 15 %
-    fewer stages than variant 1."""
+    fewer stages than variant 1.  Above 48 rows per expert the default
+    (variant 2 up to 192 rows, variant 8 above) moves when a wave model with
+    every expert at the mean predicts a 15 % gain for the other."""
     per = rows // max(E, 1)
     if per <= 48:
         if num_sms > 0 and rows <= 32 * E and K >= 512 and N >= W_TILE and split_ctas >= SPLIT_CLUSTER:
@@ -48,9 +50,22 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
                 if 20 * c6 <= 17 * c1:
                     return 6
         return 1
-    if per <= 192:
-        return 2
-    return 8
+    default = 2 if per <= 192 else 8
+    if num_sms <= 0 or N < W_TILE:
+        return default
+    # wave model with every expert at the mean; a variant-8 round costs
+    # 1.25 + 0.0026 * tile rows variant-2 rounds; moves the default only
+    # for a predicted 15 % gain
+    g = 2 * num_sms
+    blocks = E * (N // W_TILE)
+    t2 = -(-per // VARIANT_T_MAX[2])
+    t8 = -(-per // VARIANT_T_MAX[8])
+    rows8 = -(-(-(-per // t8)) // 16) * 16
+    c2 = -(-(blocks * t2) // g) * 10000
+    c8 = -(-(blocks * t8) // g) * (12500 + 26 * rows8)
+    if default == 2:
+        return 8 if 100 * c8 <= 85 * c2 else 2
+    return 2 if 100 * c8 >= 118 * c2 else 8
 
 
 def expert_tiling(rows_e: int, t_max: int = T_MAX, step: int = MMA_N_STEP):

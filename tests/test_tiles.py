@@ -58,6 +58,26 @@ def test_variant_choice_mirrors_the_library():
         hg.hg_set_gemm_variant(9)
 
 
+@pytest.mark.parametrize("E,N,K,rows,want", [
+    (12, 6144, 3584, 1024, 2),    # 85 rows per expert: one 112-row tile each, same units
+    (12, 6144, 3584, 1408, 8),    # 117: two 112-row tiles or one 224-row tile, 4 rounds vs 2
+    (12, 6144, 3584, 1792, 8),
+    (12, 3584, 3072, 1792, 2),    # 336 units of 224 rows fill 1.1 waves: the 2nd round is wasted
+    (12, 3584, 3072, 2560, 2),    # above 192 rows, still variant 2 (3 rounds vs 2 costlier ones)
+    (12, 6144, 3584, 2560, 8),
+    (32, 4096, 6144, 4096, 2),    # 128 rows per expert: 7 rounds vs 4 at 1.58x, below the margin
+    (32, 6144, 2048, 6144, 2),
+    (32, 4096, 6144, 9216, 8),
+    (32, 4096, 6144, 16384, 8),
+    (32, 6144, 2048, 131072, 8),
+])
+def test_wave_model_variant_choice(E, N, K, rows, want):
+    # with a device of 152 SMs the mean-rows default moves only where the
+    # wave model predicts a 15 % gain; without a device it never moves
+    assert T.pick_variant(E, N, rows, K, num_sms=152, split_ctas=296) == want
+    assert T.pick_variant(E, N, rows, K) == (2 if rows // E <= 192 else 8)
+
+
 def test_tile_inflation_vs_fixed_128():
     # the problem the per-expert sizing addresses: with fixed 128-row tiles,
     # experts just over 128 or 256 rows need a mostly empty extra tile
