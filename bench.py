@@ -90,6 +90,38 @@ def measured_traffic(M):
     return float(fields["dram_bytes_per_launch"])
 
 
+def host_link_gbs(cs, dev):
+    """Host<->device copy rates (GB/s) of this box with the largest batch's
+    pinned buffers: upload alone, download alone, and both at once (total)."""
+    h = cs["host"]
+    up_d = torch.empty_like(h["a"], device=dev)
+    dn_d = torch.empty_like(h["out"], device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    def up():
+        with torch.cuda.stream(s1):
+            up_d.copy_(h["a"], non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s2):
+            h["out"].copy_(dn_d, non_blocking=True)
+
+    nu, nd = h["a"].numel(), h["out"].numel() * 2
+    tu, td = timed(up), timed(down)
+    tb = timed(lambda: (up(), down()))
+    return dict(h2d=round(nu / tu / 1e9, 1), d2h=round(nd / td / 1e9, 1),
+                both=round((nu + nd) / tb / 1e9, 1))
+
+
 def algorithmic(R, E_act, E, N, K):
     """GEMM flops and the bytes each operand must cross HBM once."""
     flops = 2.0 * R * N * K
@@ -327,40 +359,37 @@ def run_ours(args, rank, world):
         sum(max(cs["bytes"] / (peaks["hbm_gbs"] * 1e9), cs["flops"] / (fp8_peak * 1e12))
             for cs in cases) / (sum(statistics.median(g) for g in gemm_us) * 1e-6), 3)
 
-    # ---- end to end: host buffers, copies inside the timed region.  The
-    # sweep's batches are independent, so uploads of batch i+1 and downloads
-    # of batch i-1 overlap the plan + GEMM of batch i (one stream each for
-    # host->device copies, compute and device->host copies).
+    # ---- end to end: every batch through hg_grouped_w4a8_gemm_host, which
+    # takes the ids, activations, scales and output in pinned host memory and
+    # makes the copies itself (ids, A and scales up, plan, GEMM, output down,
+    # all on one stream).  The sweep's batches are independent: they go to
+    # three streams in turn, so one batch's uploads overlap another's GEMM
+    # and a third's download.
     e2e = None
     if not args.no_e2e:
-        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        e_streams = [torch.cuda.Stream() for _ in range(3)]
+        for cs in cases:
+            c = cs["c"]
+            cs["host_ws"] = torch.empty(
+                hg.hg_gemm_host_workspace_bytes(c.M, c.top_k, c.E, c.N, c.K), dtype=torch.uint8,
+                device=dev)
 
         def e2e_step():
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(s_in)
-            done = []
-            for cs in cases:
-                b, h, c = cs["bufs"], cs["host"], cs["c"]
-                ev_in = torch.cuda.Event()
-                ev_out = torch.cuda.Event()
-                with torch.cuda.stream(s_in):
-                    b["ids"].copy_(h["ids"], non_blocking=True)
-                    c.a_fp8.copy_(h["a"], non_blocking=True)
-                    c.a_scale.copy_(h["a_s"], non_blocking=True)
-                    ev_in.record(s_in)
-                stream.wait_event(ev_in)
-                launch(cs, stream)
-                ev_out.record(stream)
-                s_out.wait_event(ev_out)
-                with torch.cuda.stream(s_out):
-                    h["out"].copy_(b["out"], non_blocking=True)
-                    ev_d = torch.cuda.Event()
-                    ev_d.record(s_out)
-                done.append(ev_d)
-            for ev in done:
-                s_in.wait_event(ev)
-            e1.record(s_in)
+            e0.record(stream)
+            for s in e_streams:
+                s.wait_event(e0)
+            for i, cs in enumerate(cases):
+                c, h = cs["c"], cs["host"]
+                hg.hg_grouped_w4a8_gemm_host(h["ids"], h["a"], h["a_s"], c.w_fp4, c.w_scale,
+                                             c.E, h["out"], cs["host_ws"],
+                                             stream=e_streams[i % len(e_streams)])
+            for s in e_streams:
+                ev = torch.cuda.Event()
+                ev.record(s)
+                stream.wait_event(ev)
+            e1.record(stream)
             return e0, e1
 
         for _ in range(max(1, args.warmup // 2)):
@@ -376,11 +405,14 @@ def run_ours(args, rank, world):
         flops_e2e = reduce_scalar(flops_step * e2e_steps, "sum", world)
         bi = sum(cs["c"].topk_ids.nbytes + cs["c"].a_fp8.numel() + cs["c"].a_scale.numel()
                  for cs in cases)
-        bo = sum(cs["bufs"]["out"].numel() * 2 for cs in cases)
+        bo = sum(cs["host"]["out"].numel() * 2 for cs in cases)
+        link = host_link_gbs(cases[-1], dev)
         e2e = dict(value=round(flops_e2e / tot / 1e12, 2), unit=UNIT, h2d_bytes_per_step=int(bi),
                    d2h_bytes_per_step=int(bo), ms_per_step=round(tot / e2e_steps * 1e3, 3),
-                   note="pinned host buffers; uploads, plan+GEMM and downloads of the sweep's "
-                        "independent batches overlap on three streams")
+                   host_link_gbs=link,
+                   copy_floor_ms=round((bi + bo) / (link["both"] * 1e9) * 1e3, 3),
+                   note="hg_grouped_w4a8_gemm_host per batch (pinned host buffers, the library "
+                        "copies); batches on three streams in turn")
 
     moe_io = None if args.no_moe_io else time_moe_io(cases[-1], flush, stream, peaks, hg)
 

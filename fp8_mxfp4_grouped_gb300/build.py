@@ -18,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
 LIB_PATH = os.path.join(HERE, "libhg.so")
-SOURCES = ["api.cu", "plan.cu", "gemm.cu", "moe_io.cu", "plan_noalloc.cu"]
+SOURCES = ["api.cu", "plan.cu", "gemm.cu", "moe_io.cu", "plan_noalloc.cu", "gemm_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

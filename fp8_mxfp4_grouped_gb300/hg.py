@@ -59,6 +59,11 @@ lib.hg_gemm_ctas.argtypes = [_i32, _i32, _i32, _i32]
 lib.hg_gemm_ctas.restype = _i32
 lib.hg_set_gemm_variant.argtypes = [_i32]
 lib.hg_set_gemm_variant.restype = _i32
+lib.hg_gemm_host_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
+lib.hg_gemm_host_workspace_bytes.restype = _sz
+lib.hg_grouped_w4a8_gemm_host.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p,
+                                          _p, _p, _p, _sz, _p]
+lib.hg_grouped_w4a8_gemm_host.restype = ctypes.c_int
 
 HG_OK = 0
 HG_ERR_INVALID_ARG = 1
@@ -140,6 +145,42 @@ def hg_grouped_w4a8_gemm(a_fp8: torch.Tensor, a_scale: torch.Tensor, w_fp4: torc
                                   _ptr(expert_offsets), E, N, K, rows, _ptr(out),
                                   _stream(stream))
     _check(st, "hg_grouped_w4a8_gemm")
+    return out
+
+
+def hg_gemm_host_workspace_bytes(M: int, top_k: int, E: int, N: int, K: int) -> int:
+    return int(lib.hg_gemm_host_workspace_bytes(M, top_k, E, N, K))
+
+
+def hg_grouped_w4a8_gemm_host(topk_ids: torch.Tensor, a_fp8: torch.Tensor, a_scale: torch.Tensor,
+                              w_fp4: torch.Tensor, w_scale: torch.Tensor, E: int,
+                              out: torch.Tensor, workspace: torch.Tensor,
+                              expert_offsets=None, sorted_to_src=None, stream=None):
+    """Plan + GEMM from host buffers (CPU tensors, page-locked for asynchronous
+    copies): topk_ids int32 [M, top_k], a_fp8 uint8 [M*top_k, K] in the plan's
+    order, a_scale uint8 [M*top_k, K/128], out bfloat16 [M*top_k, N]; optional
+    host outputs expert_offsets int32 [E+1] and sorted_to_src int32 [M*top_k].
+    Weights and workspace (uint8, hg_gemm_host_workspace_bytes) are on the
+    device.  Asynchronous on `stream`: the host outputs are valid once the
+    stream has reached the end of the call."""
+    M, k = topk_ids.shape
+    R = M * k
+    _, N, K2 = w_fp4.shape
+    K = 2 * K2
+    for t in (topk_ids, a_fp8, a_scale, out):
+        assert not t.is_cuda and t.is_contiguous()
+    for t in (expert_offsets, sorted_to_src):
+        assert t is None or (not t.is_cuda and t.is_contiguous())
+    assert topk_ids.dtype == torch.int32
+    assert a_fp8.shape == (R, K) and a_scale.shape == (R, K // 128) and out.shape == (R, N)
+    assert expert_offsets is None or expert_offsets.numel() == E + 1
+    assert sorted_to_src is None or sorted_to_src.numel() == R
+    assert workspace.is_cuda and workspace.dtype == torch.uint8
+    st = lib.hg_grouped_w4a8_gemm_host(_ptr(topk_ids), _ptr(a_fp8), _ptr(a_scale), _ptr(w_fp4),
+                                       _ptr(w_scale), M, k, E, N, K, _ptr(out),
+                                       _ptr(expert_offsets), _ptr(sorted_to_src), _ptr(workspace),
+                                       workspace.numel(), _stream(stream))
+    _check(st, "hg_grouped_w4a8_gemm_host")
     return out
 
 

@@ -279,6 +279,54 @@ hg_status hg_combine_topk(const uint16_t* y_bf16, const int32_t* src_to_sorted,
                           const float* topk_weights, int32_t M, int32_t top_k, int32_t N,
                           uint16_t* out_bf16, hg_stream_t stream);
 
+/* ------------------------------------------------- from host buffers -- */
+
+/*
+ * Device workspace bytes of hg_grouped_w4a8_gemm_host for these sizes (the
+ * device copies of the ids, activations, scales and output, the plan's
+ * results and the plan's own workspace, each region 256-byte aligned); 0 for
+ * M < 0, top_k < 1, E < 1, N < 1, K < 128 or M*top_k >= 2^31.
+ */
+size_t hg_gemm_host_workspace_bytes(int32_t M, int32_t top_k, int32_t E, int32_t N, int32_t K);
+
+/*
+ * The routing plan and the grouped GEMM on inputs and outputs in host
+ * memory: the same computation as hg_plan_expert_offsets followed by
+ * hg_grouped_w4a8_gemm with rows = M*top_k, with the host<->device copies
+ * made by the library.  On `stream`, in order: copies of topk_ids, a_fp8 and
+ * a_scale to the workspace; the plan; the GEMM; copies of the output (and of
+ * the offsets and sorted_to_src when those pointers are non-null) back to
+ * host memory.  The host buffers must stay valid and unchanged until the
+ * stream reaches the end of the call; they should be page-locked
+ * (cudaHostAlloc or cudaHostRegister), else the copies do not overlap other
+ * work and may block the calling thread.
+ *
+ *   topk_ids_host        int32 [M, top_k] host.
+ *   a_fp8_host           uint8 [M*top_k, K] host, E4M3 rows in the plan's order
+ *                        (sorted by expert, stable), as hg_grouped_w4a8_gemm takes.
+ *   a_scale_host         uint8 [M*top_k, K/128] host, E8M0.
+ *   w_fp4, w_scale       device, as for hg_grouped_w4a8_gemm (weights stay
+ *                        resident across calls).
+ *   out_bf16_host        uint16 [M*top_k, N] host out; rows at and beyond off[E]
+ *                        (dropped ids) are written with the workspace's
+ *                        contents and carry no result.
+ *   expert_offsets_host  int32 [E+1] host out, or NULL.
+ *   sorted_to_src_host   int32 [M*top_k] host out, or NULL.
+ *   workspace            device, at least hg_gemm_host_workspace_bytes bytes,
+ *                        256-byte aligned; one call at a time may use it.
+ *
+ * Argument errors, shapes and device-detected problems as the two calls it
+ * makes; a workspace that is missing, too small or misaligned is
+ * HG_ERR_INVALID_ARG.  Nothing is launched or copied when an argument is
+ * rejected.  No host synchronisation.
+ */
+hg_status hg_grouped_w4a8_gemm_host(const int32_t* topk_ids_host, const uint8_t* a_fp8_host,
+                                    const uint8_t* a_scale_host, const uint8_t* w_fp4,
+                                    const uint8_t* w_scale, int32_t M, int32_t top_k, int32_t E,
+                                    int32_t N, int32_t K, uint16_t* out_bf16_host,
+                                    int32_t* expert_offsets_host, int32_t* sorted_to_src_host,
+                                    void* workspace, size_t workspace_bytes, hg_stream_t stream);
+
 /* ------------------------------------------------------------- status -- */
 
 /*

@@ -128,3 +128,46 @@ def test_quantize_scatter_argument_validation(lib):
     assert call(x=0x1008) == lib.HG_ERR_INVALID_ARG                # 16-byte alignment
     assert call(a=0x3008) == lib.HG_ERR_INVALID_ARG
     assert call(M=0, x=0, d2s=0, a=0, s=0) == lib.HG_OK            # empty: a no-op
+
+
+def test_gemm_host_workspace_bytes(lib):
+    f = lib.hg_gemm_host_workspace_bytes
+    # regions (each rounded up to 256 bytes): ids R*4, offsets (E+1)*4,
+    # sorted_to_src R*4, src_to_sorted R*4, plan workspace, A R*K,
+    # scales R*K/128, out R*N*2
+    R, E, N, K = 32, 4, 256, 512
+    assert lib.hg_plan_workspace_bytes(16, 2, E) == 16
+    assert f(16, 2, E, N, K) == 256 * 6 + R * K + R * N * 2
+    assert f(0, 8, 32, 4096, 6144) == 256 + 256          # offsets and the plan's counts
+    big = f(16384, 8, 32, 4096, 6144)
+    R = 16384 * 8
+    assert big >= R * (4 * 3 + 6144 + 48 + 4096 * 2) and big % 256 == 0
+    assert f(-1, 8, 32, 256, 512) == 0 and f(4, 0, 32, 256, 512) == 0
+    assert f(4, 8, 0, 256, 512) == 0 and f(4, 8, 32, 0, 512) == 0 and f(4, 8, 32, 256, 64) == 0
+
+
+def test_gemm_host_argument_validation(lib):
+    c = ctypes.c_void_p
+    f = lib.lib.hg_grouped_w4a8_gemm_host
+    need = lib.hg_gemm_host_workspace_bytes(4, 8, 32, 256, 512)
+    ok = dict(ids=0x1000, a=0x2000, s=0x3000, w=0x4000, ws_=0x5000, M=4, k=8, E=32, N=256, K=512,
+              out=0x6000, off=0x7000, s2s=0x8000, wk=0x10000, wkb=need)
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(c(a["ids"]), c(a["a"]), c(a["s"]), c(a["w"]), c(a["ws_"]), a["M"], a["k"], a["E"],
+                 a["N"], a["K"], c(a["out"]), c(a["off"]), c(a["s2s"]), c(a["wk"]), a["wkb"], None)
+    assert call(M=-1) == lib.HG_ERR_INVALID_ARG
+    assert call(k=0) == lib.HG_ERR_INVALID_ARG
+    assert call(E=0) == lib.HG_ERR_INVALID_ARG
+    assert call(E=513) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert call(N=200) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert call(K=384) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert call(M=1 << 30) == lib.HG_ERR_UNSUPPORTED_SHAPE      # M*top_k >= 2^31
+    assert call(w=0x4010) == lib.HG_ERR_INVALID_ARG              # W needs 32-byte alignment
+    assert call(ws_=0x5001) == lib.HG_ERR_INVALID_ARG
+    assert call(ids=0) == lib.HG_ERR_INVALID_ARG
+    assert call(a=0) == lib.HG_ERR_INVALID_ARG
+    assert call(out=0) == lib.HG_ERR_INVALID_ARG
+    assert call(wk=0) == lib.HG_ERR_INVALID_ARG
+    assert call(wk=0x10010) == lib.HG_ERR_INVALID_ARG            # workspace 256-byte aligned
+    assert call(wkb=need - 1) == lib.HG_ERR_INVALID_ARG
