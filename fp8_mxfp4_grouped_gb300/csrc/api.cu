@@ -169,7 +169,7 @@ hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top
     a.threads = threads;
     a.nblk = nblk;
     a.chunk = static_cast<int>(chunk);
-    a.small = plan_small_fits(a.R, E, d->smem_optin);
+    a.cluster_ctas = plan_cluster_ctas(a.R, E, d->smem_optin);
     return launch_plan(a, s) == cudaSuccess ? HG_OK : HG_ERR_CUDA;
 }
 

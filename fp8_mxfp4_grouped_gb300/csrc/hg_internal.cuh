@@ -112,12 +112,14 @@ struct PlanArgs {
     int threads;   // block size chosen by the shared-memory fit
     int nblk;      // number of blocks of the histogram / scatter grids
     int chunk;     // ids per block (multiple of 32)
-    bool small;    // whole plan in one 1024-thread block (plan_small_fits)
+    int cluster_ctas;   // > 0: whole plan in one cluster of this many CTAs (plan_cluster_ctas)
 };
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 size_t plan_smem_bytes(int32_t E, int threads);
-bool plan_small_fits(int32_t R, int32_t E, int smem_limit);
+// CTAs of the one-cluster plan for R routed rows and E experts (1..8), or 0
+// when R or the count tables exceed what one cluster holds.
+int plan_cluster_ctas(int32_t R, int32_t E, int smem_limit);
 
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 

@@ -8,12 +8,15 @@
 // contiguous one of humming PR #129 ("perf(sm90): size grouped W4A8 tiles
 // per expert", first section): each expert's rows form one range.
 //
-// Up to 6144 routed rows (and E small enough for a 32-warp count table) the
-// whole plan is ONE block of 1024 threads (plan_small): each warp keeps its
-// contiguous sub-chunk of ids in registers, counts it, and after one scan
-// places it.  Larger inputs take two launches:
+// Up to 32768 routed rows (and E small enough for a 32-warp count table) the
+// whole plan is ONE launch of one thread-block cluster (plan_cluster, up to
+// 8 CTAs): each warp keeps its contiguous sub-chunk of ids in registers,
+// counts it, the CTAs exchange their per-expert totals through distributed
+// shared memory, and each warp places its ids.  Larger inputs take two
+// launches:
 //   plan_hist:    block b counts the ids of its chunk per expert
-//                 (warp-aggregated with __match_any_sync) -> ws[b][e].
+//                 (warp-aggregated: the lanes holding equal ids are found
+//                 with one ballot per bit of the id) -> ws[b][e].
 //   plan_scatter: every block rebuilds the exclusive scan over (expert,
 //                 block) from ws, block 0 writes expert_offsets, then each
 //                 warp places its contiguous sub-chunk in order: the rank of
@@ -21,6 +24,7 @@
 //                 lower lanes, so the order inside an expert is ascending
 //                 source index (stable).
 #include "hg_internal.cuh"
+#include "ptx.cuh"
 
 namespace hg {
 namespace {
@@ -28,6 +32,21 @@ namespace {
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Lanes of the warp whose key equals this lane's, for keys in [0, 2^nbits)
+// and negative keys (all negative keys of the warp share one class here,
+// separate from the valid ones).  Every lane of the warp must call it with
+// the same nbits.
+__device__ __forceinline__ uint32_t lanes_with_equal_key(int key, int nbits) {
+    uint32_t m = __ballot_sync(0xFFFFFFFFu, key < 0);
+    if (key >= 0) m = ~m;
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, bit);
+        m &= bit ? bal : ~bal;
+    }
     return m;
 }
 
@@ -41,6 +60,7 @@ __global__ void plan_hist_kernel(const int32_t* __restrict__ ids, int R, int E, 
     const int begin = blockIdx.x * chunk;
     const int end = min(R, begin + chunk);
     uint32_t bad = 0;
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
     for (int base = begin + (threadIdx.x & ~31); base < end; base += blockDim.x) {
         const int i = base + lane;
         int key = -2;   // padding lane
@@ -48,7 +68,7 @@ __global__ void plan_hist_kernel(const int32_t* __restrict__ ids, int R, int E, 
             const int e = __ldg(ids + i);
             key = (e >= 0 && e < E) ? e : -1;
         }
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+        const uint32_t peers = lanes_with_equal_key(key, nbits);
         if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[key], __popc(peers));
         if (key == -1) ++bad;
     }
@@ -96,6 +116,7 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ ids, int R, int 
     const int wbeg = begin + warp * sub;
     const int wend = min(end, wbeg + sub);
     int32_t* mycnt = wc + static_cast<size_t>(warp) * E;
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
     for (int s0 = wbeg; s0 < wend; s0 += 32) {
         const int i = s0 + lane;
         int key = -2;
@@ -103,7 +124,7 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ ids, int R, int 
             const int e = __ldg(ids + i);
             key = (e >= 0 && e < E) ? e : -1;
         }
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+        const uint32_t peers = lanes_with_equal_key(key, nbits);
         if (key >= 0 && lane == __ffs(peers) - 1) mycnt[key] += __popc(peers);
     }
     __syncthreads();
@@ -154,7 +175,7 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ ids, int R, int 
             const int e = __ldg(ids + i);
             key = (e >= 0 && e < E) ? e : -1;
         }
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+        const uint32_t peers = lanes_with_equal_key(key, nbits);
         int dest = -1;
         if (key >= 0) dest = mycnt[key] + __popc(peers & lt);
         __syncwarp();
@@ -173,38 +194,61 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ ids, int R, int 
 }
 
 
-#ifndef HG_PLAN_SMALL_MAX_R
-#define HG_PLAN_SMALL_MAX_R 6144
-#endif
-constexpr int kSmallThreads = 1024;
-constexpr int kSmallIdsPerLane = 16;
-constexpr int kSmallMaxR = HG_PLAN_SMALL_MAX_R;
-static_assert(kSmallMaxR <= kSmallThreads * kSmallIdsPerLane, "ids must fit the registers");
+// ---------------------------------------------------- one cluster --
+//
+// Up to kClusterMaxR routed rows (and E small enough for the count tables)
+// the whole plan is ONE launch: a cluster of up to 8 CTAs of 1024 threads.
+// CTA c of the cluster owns a contiguous chunk of the ids, each of its warps
+// a contiguous sub-chunk, held in registers (at most kClusterIdsPerLane per
+// lane).  Each warp counts its sub-chunk per expert; the lanes holding equal
+// ids are found with one warp ballot per bit of the id (plus one for
+// validity), and those masks are kept for the placing pass.  Each CTA then
+// turns its per-warp counts into per-warp exclusive prefixes and totals;
+// after a cluster barrier every CTA reads all CTAs' totals from their shared
+// memory, so it knows the expert offsets and how many ids of each expert the
+// lower CTAs hold; a second barrier lets the CTAs go on without their totals
+// being read any more.  The placing pass gives id i of expert e the row
+// off[e] + (ids of e in lower CTAs, lower warps, earlier warp steps and lower
+// lanes): ascending source index inside each expert.
+constexpr int kClusterThreads = 1024;
+constexpr int kClusterWarps = kClusterThreads / 32;
+constexpr int kClusterIdsPerLane = 4;
+constexpr int kClusterMaxCtas = 8;
+constexpr int kClusterIdsPerCta = kClusterThreads * kClusterIdsPerLane;
+constexpr int kClusterMaxR = kClusterMaxCtas * kClusterIdsPerCta;
 
-// Shared memory: per-warp table wc[32][E], base[E], then the permutation
-// sorted_to_src itself (R entries): placing rows in shared memory and writing
-// the array out once, coalesced, avoids R scattered 4-byte global stores
-// from a single SM.
-__global__ void __launch_bounds__(kSmallThreads)
-plan_small_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
-                  int32_t* __restrict__ sorted_to_src, int32_t* __restrict__ src_to_sorted,
-                  uint32_t* status) {
-    extern __shared__ int32_t sm_small[];
-    constexpr int nw = kSmallThreads / 32;
+// Shared memory: per-warp count table wc[32][E] (then per-warp exclusive
+// prefixes), then the CTA's totals, the cluster totals and the CTA's bases,
+// E entries each.
+__global__ void __launch_bounds__(kClusterThreads)
+plan_cluster_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ sorted_to_src, int32_t* __restrict__ src_to_sorted,
+                    uint32_t* status) {
+    extern __shared__ int32_t sm_cl[];
+    constexpr int nw = kClusterWarps;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    int32_t* wc = sm_small;                        // [nw][E]
-    int32_t* base = wc + nw * E;                   // [E]
-    int32_t* s2d = base + E;                       // [R]
+    const int crank = static_cast<int>(ptx::cluster_ctarank());
+    const int csize = static_cast<int>(ptx::cluster_nctarank());
+    int32_t* wc = sm_cl;                 // [nw][E]
+    int32_t* cta_cnt = wc + nw * E;      // [E] ids of each expert in this CTA
+    int32_t* tot = cta_cnt + E;          // [E] ids of each expert in the cluster
+    int32_t* base = tot + E;             // [E] first row of this CTA's ids of each expert
     __shared__ int32_t s_total;
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
 
-    // Contiguous sub-chunk per warp, a multiple of 32 ids long.
-    const int sub = ((R + nw - 1) / nw + 31) & ~31;
-    const int wbeg = warp * sub;
-    const int wend = min(R, wbeg + sub);
-    int key[kSmallIdsPerLane];
+    // This CTA's chunk and this warp's sub-chunk, multiples of 32 ids; every
+    // CTA computes the same chunk length.
+    const int csz = ((R + csize - 1) / csize + 31) & ~31;
+    const int cbeg = crank * csz;
+    const int cend = min(R, cbeg + csz);
+    const int sub = ((csz + nw - 1) / nw + 31) & ~31;
+    const int wbeg = cbeg + warp * sub;
+    const int wend = min(cend, wbeg + sub);
+    int key[kClusterIdsPerLane];
+    uint32_t peers[kClusterIdsPerLane];
 #pragma unroll
-    for (int j = 0; j < kSmallIdsPerLane; ++j) {
+    for (int j = 0; j < kClusterIdsPerLane; ++j) {
         const int i = wbeg + 32 * j + lane;
         key[j] = -2;
         if (32 * j < sub && i < wend) {
@@ -212,16 +256,17 @@ plan_small_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __rest
             key[j] = (e >= 0 && e < E) ? e : -1;
         }
     }
-    for (int i = threadIdx.x; i < (nw + 1) * E; i += kSmallThreads) sm_small[i] = 0;
+    for (int i = threadIdx.x; i < nw * E; i += kClusterThreads) sm_cl[i] = 0;
     __syncthreads();
 
     int32_t* mycnt = wc + warp * E;
     uint32_t bad = 0;
 #pragma unroll
-    for (int j = 0; j < kSmallIdsPerLane; ++j) {
+    for (int j = 0; j < kClusterIdsPerLane; ++j) {
+        peers[j] = 0;
         if (32 * j < sub) {
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key[j]);
-            if (key[j] >= 0 && lane == __ffs(peers) - 1) mycnt[key[j]] += __popc(peers);
+            peers[j] = lanes_with_equal_key(key[j], nbits);
+            if (key[j] >= 0 && lane == __ffs(peers[j]) - 1) mycnt[key[j]] += __popc(peers[j]);
             if (key[j] == -1) ++bad;
         }
     }
@@ -230,17 +275,40 @@ plan_small_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __rest
         record_error(status, HG_ERR_BAD_IDS, 0u);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kSmallThreads) {
-        int t = 0;
-        for (int w = 0; w < nw; ++w) t += wc[w * E + e];
-        base[e] = t;
+    // per-warp exclusive prefixes and the CTA's totals, one expert per thread
+    for (int e = threadIdx.x; e < E; e += kClusterThreads) {
+        int run = 0;
+#pragma unroll 8
+        for (int w = 0; w < nw; ++w) {
+            const int c = wc[w * E + e];
+            wc[w * E + e] = run;
+            run += c;
+        }
+        cta_cnt[e] = run;
     }
-    __syncthreads();
+    // every CTA's totals are complete and visible to the cluster
+    __syncwarp();
+    ptx::cluster_sync();
+    const uint32_t cnt_saddr = static_cast<uint32_t>(__cvta_generic_to_shared(cta_cnt));
+    for (int e = threadIdx.x; e < E; e += kClusterThreads) {
+        int lower = 0, all = 0;
+        for (int c = 0; c < csize; ++c) {
+            const int v = static_cast<int>(ptx::ld_shared_cluster_u32(
+                ptx::mapa_shared(cnt_saddr + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(c))));
+            if (c < crank) lower += v;
+            all += v;
+        }
+        base[e] = lower;
+        tot[e] = all;
+    }
+    // no CTA's totals are read after this point: each CTA may go on and exit
+    __syncwarp();
+    ptx::cluster_sync();
     if (warp == 0) {
         int carry = 0;
         for (int c = 0; c < E; c += 32) {
             const int e = c + lane;
-            const int v = e < E ? base[e] : 0;
+            const int v = e < E ? tot[e] : 0;
             int incl = v;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -248,57 +316,51 @@ plan_small_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __rest
                 if (lane >= d) incl += y;
             }
             if (e < E) {
-                offsets[e] = carry + incl - v;
-                base[e] = carry + incl - v;
+                if (crank == 0) offsets[e] = carry + incl - v;
+                base[e] += carry + incl - v;
             }
             carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         if (lane == 0) {
-            offsets[E] = carry;
+            if (crank == 0) offsets[E] = carry;
             s_total = carry;
-        }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kSmallThreads) {
-        int run = base[e];
-        for (int w = 0; w < nw; ++w) {
-            const int c = wc[w * E + e];
-            wc[w * E + e] = run;
-            run += c;
         }
     }
     __syncthreads();
     const uint32_t lt = lanemask_lt();
 #pragma unroll
-    for (int j = 0; j < kSmallIdsPerLane; ++j) {
+    for (int j = 0; j < kClusterIdsPerLane; ++j) {
         if (32 * j < sub) {
             const int i = wbeg + 32 * j + lane;
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key[j]);
             int dest = -1;
-            if (key[j] >= 0) dest = mycnt[key[j]] + __popc(peers & lt);
+            if (key[j] >= 0) dest = base[key[j]] + mycnt[key[j]] + __popc(peers[j] & lt);
             __syncwarp();
-            if (key[j] >= 0 && lane == __ffs(peers) - 1) mycnt[key[j]] += __popc(peers);
+            if (key[j] >= 0 && lane == __ffs(peers[j]) - 1) mycnt[key[j]] += __popc(peers[j]);
             __syncwarp();
             if (i < wend) {
                 src_to_sorted[i] = dest;
-                if (dest >= 0) s2d[dest] = i;
+                if (dest >= 0) sorted_to_src[dest] = i;
             }
         }
     }
-    __syncthreads();
+    // Rows past the last placed one (only when ids were dropped).
     const int total = s_total;
-    for (int j = threadIdx.x; j < R; j += kSmallThreads) sorted_to_src[j] = j < total ? s2d[j] : -1;
+    for (int j = total + crank * kClusterThreads + static_cast<int>(threadIdx.x); j < R;
+         j += csize * kClusterThreads) {
+        sorted_to_src[j] = -1;
+    }
 }
 
 }  // namespace
 
-size_t plan_small_smem_bytes(int32_t R, int32_t E) {
-    return (static_cast<size_t>(kSmallThreads / 32 + 1) * static_cast<size_t>(E) +
-            static_cast<size_t>(R)) * sizeof(int32_t);
+size_t plan_cluster_smem_bytes(int32_t E) {
+    return static_cast<size_t>(kClusterWarps + 3) * static_cast<size_t>(E) * sizeof(int32_t);
 }
 
-bool plan_small_fits(int32_t R, int32_t E, int smem_limit) {
-    return R <= kSmallMaxR && plan_small_smem_bytes(R, E) <= static_cast<size_t>(smem_limit);
+int plan_cluster_ctas(int32_t R, int32_t E, int smem_limit) {
+    if (R > kClusterMaxR || plan_cluster_smem_bytes(E) > static_cast<size_t>(smem_limit)) return 0;
+    const int n = (R + kClusterIdsPerCta - 1) / kClusterIdsPerCta;
+    return n < 1 ? 1 : n;
 }
 
 size_t plan_smem_bytes(int32_t E, int threads) {
@@ -306,18 +368,34 @@ size_t plan_smem_bytes(int32_t E, int threads) {
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
-    if (a.small) {
-        const size_t smem = plan_small_smem_bytes(a.R, a.E);
+    if (a.cluster_ctas > 0) {
+        const size_t smem = plan_cluster_smem_bytes(a.E);
         if (smem > 48 * 1024) {
-            cudaError_t err = cudaFuncSetAttribute(plan_small_kernel,
+            cudaError_t err = cudaFuncSetAttribute(plan_cluster_kernel,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
             if (err != cudaSuccess) return err;
         }
-        plan_small_kernel<<<1, kSmallThreads, smem, stream>>>(a.ids, a.R, a.E, a.offsets,
-                                                               a.sorted_to_src, a.src_to_sorted,
-                                                               a.status);
-        return cudaGetLastError();
+        if (a.cluster_ctas == 1) {
+            // one CTA: a plain launch (a cluster of one is implicit)
+            plan_cluster_kernel<<<1, kClusterThreads, smem, stream>>>(
+                a.ids, a.R, a.E, a.offsets, a.sorted_to_src, a.src_to_sorted, a.status);
+            return cudaGetLastError();
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(a.cluster_ctas), 1, 1);
+        cfg.blockDim = dim3(kClusterThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(a.cluster_ctas);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, plan_cluster_kernel, a.ids, a.R, a.E, a.offsets,
+                                  a.sorted_to_src, a.src_to_sorted, a.status);
     }
     const size_t smem_hist = static_cast<size_t>(a.E) * sizeof(int32_t);
     const size_t smem_scat = plan_smem_bytes(a.E, a.threads);

@@ -75,3 +75,33 @@ def test_plan_deterministic(cuda_lib):
     b = _gpu_plan(cuda_lib, ids, 32)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("M,k,E", [
+    (512, 8, 32),      # 4096 ids: one CTA
+    (4097, 1, 5),      # 4097 ids: two CTAs, the second holding one warp step
+    (4096, 8, 33),     # 32768 ids: eight CTAs, four ids per lane
+    (32769, 1, 12),    # one id more than one cluster holds: two launches
+    (8192, 8, 12),     # 65536 ids: two launches
+    (1000, 8, 1500),   # count tables above 48 KB of shared memory
+    (3, 3, 2),         # fewer ids than one warp step
+])
+def test_plan_cluster_boundaries(cuda_lib, M, k, E):
+    rng = np.random.default_rng(M + 31 * E)
+    ids = rng.integers(0, E, (M, k)).astype(np.int32)
+    off, s2d, d2s = _gpu_plan(cuda_lib, ids, E)
+    r_off, r_s2d, r_d2s, _ = plan_expert_offsets(ids, E)
+    assert np.array_equal(off, r_off) and np.array_equal(s2d, r_s2d) and np.array_equal(d2s, r_d2s)
+
+
+def test_plan_out_of_range_ids_across_ctas(cuda_lib):
+    # dropped ids in every CTA of a multi-CTA plan: rows past off[E] are -1
+    cuda_lib.hg_get_device_status()
+    rng = np.random.default_rng(5)
+    ids = rng.integers(-2, 14, (2500, 8)).astype(np.int32)     # E = 12: -2, -1, 12, 13 dropped
+    off, s2d, d2s = _gpu_plan(cuda_lib, ids, 12)
+    r_off, r_s2d, r_d2s, bad = plan_expert_offsets(ids, 12)
+    assert bad > 0
+    assert np.array_equal(off, r_off) and np.array_equal(s2d, r_s2d) and np.array_equal(d2s, r_d2s)
+    st, detail = cuda_lib.hg_get_device_status()
+    assert st == cuda_lib.HG_ERR_BAD_IDS and detail == bad
