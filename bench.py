@@ -435,7 +435,8 @@ def run_ours(args, rank, world):
         "moe_io": moe_io,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * len(cases) * args.steps,
+        "gpu_launches": sum(hg.hg_plan_launches(cs["M"], cs["c"].top_k, cs["c"].E) + 1
+                            for cs in cases) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
     }

@@ -129,6 +129,17 @@ int32_t hg_plan_block_threads(int32_t E, int32_t smem_limit_bytes) {
     return 0;
 }
 
+int32_t hg_plan_launches(int32_t M, int32_t top_k, int32_t E) {
+    if (M < 0 || top_k < 1 || E < 1) return -1;
+    const long long R = static_cast<long long>(M) * top_k;
+    if (R > 0x7FFFFFFFll) return -1;
+    if (R == 0) return 0;
+    DeviceInfo* d = nullptr;
+    if (device_info(&d) != HG_OK) return -1;
+    if (plan_cluster_ctas(static_cast<int32_t>(R), E, d->smem_optin) > 0) return 1;
+    return hg_plan_block_threads(E, d->smem_optin) > 0 ? 2 : -1;
+}
+
 hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t E,
                                  int32_t* expert_offsets, int32_t* sorted_to_src,
                                  int32_t* src_to_sorted, void* workspace, size_t workspace_bytes,

@@ -35,6 +35,8 @@ lib.hg_plan_workspace_bytes.argtypes = [_i32, _i32, _i32]
 lib.hg_plan_workspace_bytes.restype = _sz
 lib.hg_plan_block_threads.argtypes = [_i32, _i32]
 lib.hg_plan_block_threads.restype = _i32
+lib.hg_plan_launches.argtypes = [_i32, _i32, _i32]
+lib.hg_plan_launches.restype = _i32
 lib.hg_plan_expert_offsets.argtypes = [_p, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]
 lib.hg_plan_expert_offsets.restype = ctypes.c_int
 lib.hg_grouped_w4a8_gemm.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _p]
@@ -102,6 +104,10 @@ def hg_plan_workspace_bytes(M: int, top_k: int, E: int) -> int:
 
 def hg_plan_block_threads(E: int, smem_limit_bytes: int) -> int:
     return int(lib.hg_plan_block_threads(E, smem_limit_bytes))
+
+
+def hg_plan_launches(M: int, top_k: int, E: int) -> int:
+    return int(lib.hg_plan_launches(M, top_k, E))
 
 
 def hg_plan_expert_offsets(topk_ids: torch.Tensor, E: int, expert_offsets=None,

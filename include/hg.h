@@ -89,14 +89,26 @@ int32_t hg_plan_block_threads(int32_t E, int32_t smem_limit_bytes);
  *
  * Ids outside [0, E) are dropped from the layout and counted; the count is
  * reported by hg_get_device_status as HG_ERR_BAD_IDS.  M = 0 writes zero
- * offsets.  Results are bit-exact and deterministic.  Up to 6144 routed
- * rows the plan is one single-block kernel; beyond that, two kernels.
- * Launches on `stream`; no host synchronisation.
+ * offsets.  Results are bit-exact and deterministic.  Up to 32768 routed
+ * rows (and E small enough for the count tables of one CTA) the plan is one
+ * launch of one thread-block cluster; beyond that, two kernels
+ * (hg_plan_launches tells which).  Launches on `stream`; no host
+ * synchronisation.
  */
 hg_status hg_plan_expert_offsets(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t E,
                                  int32_t* expert_offsets, int32_t* sorted_to_src,
                                  int32_t* src_to_sorted, void* workspace, size_t workspace_bytes,
                                  hg_stream_t stream);
+
+/*
+ * Kernel launches hg_plan_expert_offsets makes for these sizes on the
+ * current device: 1 (the whole plan in one thread-block cluster, up to 32768
+ * routed rows when the count tables fit) or 2 (histogram, then scatter);
+ * 0 when M*top_k == 0 (the offsets are cleared with one memset); -1 for
+ * arguments the plan rejects or when the device cannot be queried.
+ * Host-only: launches nothing.
+ */
+int32_t hg_plan_launches(int32_t M, int32_t top_k, int32_t E);
 
 /*
  * The routing plan without a workspace argument, for callers that cannot

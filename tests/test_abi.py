@@ -171,3 +171,13 @@ def test_gemm_host_argument_validation(lib):
     assert call(wk=0) == lib.HG_ERR_INVALID_ARG
     assert call(wk=0x10010) == lib.HG_ERR_INVALID_ARG            # workspace 256-byte aligned
     assert call(wkb=need - 1) == lib.HG_ERR_INVALID_ARG
+
+
+def test_plan_launches_rejects_bad_arguments_without_a_device(lib):
+    # argument checks come first; sizes that need the device's limits read -1
+    # here only when no device can be queried
+    assert lib.hg_plan_launches(-1, 8, 32) == -1
+    assert lib.hg_plan_launches(4, 0, 32) == -1
+    assert lib.hg_plan_launches(4, 8, 0) == -1
+    assert lib.hg_plan_launches(0, 8, 32) == 0
+    assert lib.hg_plan_launches(1 << 30, 8, 32) == -1

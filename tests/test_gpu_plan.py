@@ -105,3 +105,12 @@ def test_plan_out_of_range_ids_across_ctas(cuda_lib):
     assert np.array_equal(off, r_off) and np.array_equal(s2d, r_s2d) and np.array_equal(d2s, r_d2s)
     st, detail = cuda_lib.hg_get_device_status()
     assert st == cuda_lib.HG_ERR_BAD_IDS and detail == bad
+
+
+def test_plan_launch_count(cuda_lib):
+    assert cuda_lib.hg_plan_launches(0, 8, 32) == 0
+    assert cuda_lib.hg_plan_launches(64, 8, 32) == 1
+    assert cuda_lib.hg_plan_launches(4096, 8, 32) == 1          # 32768 ids: one cluster
+    assert cuda_lib.hg_plan_launches(4097, 8, 32) == 2
+    assert cuda_lib.hg_plan_launches(1000, 8, 3000) == 2        # count tables beyond one CTA
+    assert cuda_lib.hg_plan_launches(-1, 8, 32) == -1
