@@ -85,6 +85,21 @@ struct GemmArgs {
     int variant;   // 1 small tiles / 2 CTAs per SM, 2 mid, 3 large tiles / 1 CTA per SM, 4 CTA pairs
 };
 
+// Lanes of the warp whose key equals this lane's, for keys in [0, 2^nbits)
+// and negative keys (all negative keys of the warp share one class here,
+// separate from the valid ones).  Every lane of the warp must call it with
+// the same nbits.
+__device__ __forceinline__ uint32_t lanes_with_equal_key(int key, int nbits) {
+    uint32_t m = __ballot_sync(0xFFFFFFFFu, key < 0);
+    if (key >= 0) m = ~m;
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+}
+
 // Activation tensor maps over the same [rows, K] bytes, 128-byte swizzle,
 // with boxes of 128 K x (16 << i) rows: any multiple of 16 rows up to 240
 // loads in at most four boxes (one TMA instruction each).

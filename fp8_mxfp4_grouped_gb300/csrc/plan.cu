@@ -35,21 +35,6 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-// Lanes of the warp whose key equals this lane's, for keys in [0, 2^nbits)
-// and negative keys (all negative keys of the warp share one class here,
-// separate from the valid ones).  Every lane of the warp must call it with
-// the same nbits.
-__device__ __forceinline__ uint32_t lanes_with_equal_key(int key, int nbits) {
-    uint32_t m = __ballot_sync(0xFFFFFFFFu, key < 0);
-    if (key >= 0) m = ~m;
-    for (int b = 0; b < nbits; ++b) {
-        const bool bit = (key >> b) & 1;
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, bit);
-        m &= bit ? bal : ~bal;
-    }
-    return m;
-}
-
 __global__ void plan_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int chunk,
                                  int32_t* __restrict__ ws, uint32_t* status) {
     extern __shared__ int32_t sm_hist[];
