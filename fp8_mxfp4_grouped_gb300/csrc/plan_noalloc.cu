@@ -2,7 +2,7 @@
 // memory.
 //
 // hg_plan_expert_offsets needs a device workspace for its two-launch path
-// (more than 6144 routed rows, or many experts): one count per block per
+// (more than 32768 routed rows, or many experts): one count per block per
 // expert.  Some callers cannot provide one, because they cannot call
 // cudaMalloc at the point where they plan: code that runs while a CUDA graph
 // is being captured (an allocation is not a stream operation, so it cannot be
