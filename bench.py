@@ -19,6 +19,7 @@ workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -303,6 +304,7 @@ def run_ours(args, rank, world):
     recs = []
     barrier(world)
     torch.cuda.synchronize()
+    gc.disable()   # no collector pause inside the timed region
     t_wall0 = time.perf_counter()
     torch.cuda.nvtx.range_push("timed")      # lets a profiler select exactly these launches
     for _ in range(args.steps):
@@ -311,6 +313,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     barrier(world)
     t_wall = time.perf_counter() - t_wall0
+    gc.enable()
     clk = clocks.stop()
 
     plan_us = [[] for _ in cases]
@@ -374,9 +377,12 @@ def run_ours(args, rank, world):
                 hg.hg_gemm_host_workspace_bytes(c.M, c.top_k, c.E, c.N, c.K), dtype=torch.uint8,
                 device=dev)
 
-        def e2e_step():
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
+        def e2e_events():
+            return (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                    [torch.cuda.Event() for _ in e_streams])
+
+        def e2e_step(events):
+            e0, e1, ends = events
             e0.record(stream)
             for s in e_streams:
                 s.wait_event(e0)
@@ -385,22 +391,24 @@ def run_ours(args, rank, world):
                 hg.hg_grouped_w4a8_gemm_host(h["ids"], h["a"], h["a_s"], c.w_fp4, c.w_scale,
                                              c.E, h["out"], cs["host_ws"],
                                              stream=e_streams[i % len(e_streams)])
-            for s in e_streams:
-                ev = torch.cuda.Event()
+            for s, ev in zip(e_streams, ends):
                 ev.record(s)
                 stream.wait_event(ev)
             e1.record(stream)
             return e0, e1
 
-        for _ in range(max(1, args.warmup // 2)):
-            e2e_step()
+        for _ in range(max(3, args.warmup)):
+            e2e_step(e2e_events())
         torch.cuda.synchronize()
         tot = 0.0
         e2e_steps = min(args.steps, 20)
-        for _ in range(e2e_steps):
-            e0, e1 = e2e_step()
+        events = [e2e_events() for _ in range(e2e_steps)]
+        gc.disable()   # no collector pause inside the timed steps
+        for k in range(e2e_steps):
+            e0, e1 = e2e_step(events[k])
             torch.cuda.synchronize()
             tot += e0.elapsed_time(e1) * 1e-3
+        gc.enable()
         tot = reduce_scalar(tot, "max", world)
         flops_e2e = reduce_scalar(flops_step * e2e_steps, "sum", world)
         bi = sum(cs["c"].topk_ids.nbytes + cs["c"].a_fp8.numel() + cs["c"].a_scale.numel()
