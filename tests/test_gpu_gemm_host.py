@@ -89,3 +89,49 @@ def test_optional_outputs_and_empty_batch(cuda_lib):
                                        expert_offsets=off0)
     torch.cuda.synchronize()
     assert torch.equal(off0, torch.zeros(E + 1, dtype=torch.int32))
+
+
+def test_pageable_host_buffers(cuda_lib):
+    # not page-locked: the copies are staged by the driver, the results are the same
+    c = make_case(2, 64, projection="down", routing="biased")
+    R = c.M * c.top_k
+    out = torch.empty((R, c.N), dtype=torch.bfloat16)
+    ws = torch.empty(cuda_lib.hg_gemm_host_workspace_bytes(c.M, c.top_k, c.E, c.N, c.K),
+                     dtype=torch.uint8, device="cuda")
+    cuda_lib.hg_grouped_w4a8_gemm_host(torch.from_numpy(np.ascontiguousarray(c.topk_ids)),
+                                       c.a_fp8.cpu().contiguous(), c.a_scale.cpu().contiguous(),
+                                       c.w_fp4.cuda(), c.w_scale.cuda(), c.E, out, ws)
+    torch.cuda.synchronize()
+    out_d, _, _ = _device_calls(cuda_lib, c)
+    assert torch.equal(out.view(torch.int16), out_d.view(torch.int16))
+
+
+def test_graph_capture_and_replay(cuda_lib):
+    # the whole host-buffer call captured once; replays read the pinned inputs
+    # as they are at replay time and write the pinned output
+    c1 = make_case(1, 64, projection="gate_up", routing="biased")
+    c2 = make_case(1, 64, projection="gate_up", routing="uniform")
+    R = c1.M * c1.top_k
+    ids = _pinned(torch.from_numpy(np.ascontiguousarray(c1.topk_ids)))
+    a = _pinned(c1.a_fp8.cpu())
+    a_s = _pinned(c1.a_scale.cpu())
+    out = torch.empty((R, c1.N), dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(cuda_lib.hg_gemm_host_workspace_bytes(c1.M, c1.top_k, c1.E, c1.N, c1.K),
+                     dtype=torch.uint8, device="cuda")
+    w, w_s = c1.w_fp4.cuda(), c1.w_scale.cuda()
+    s = torch.cuda.Stream()
+    cuda_lib.hg_grouped_w4a8_gemm_host(ids, a, a_s, w, w_s, c1.E, out, ws, stream=s)   # warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cuda_lib.hg_grouped_w4a8_gemm_host(ids, a, a_s, w, w_s, c1.E, out, ws,
+                                           stream=torch.cuda.current_stream())
+    for c in (c2, c1):
+        ids.copy_(torch.from_numpy(np.ascontiguousarray(c.topk_ids)))
+        a.copy_(c.a_fp8.cpu())
+        a_s.copy_(c.a_scale.cpu())
+        g.replay()
+        torch.cuda.synchronize()
+        out_d, _, _ = _device_calls(cuda_lib, c)
+        assert torch.equal(out.view(torch.int16), out_d.view(torch.int16))
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
