@@ -231,7 +231,7 @@ def run_ours(args, rank, world):
     from synth.inputs import CONFIGS
 
     dev = torch.device("cuda")
-    cfg = CONFIGS[CONFIG_ID]
+    cfg = CONFIGS[args.config]
     Ms = args.Ms or cfg["Ms"]
     peaks = load_peaks()
     fp8_peak = peaks["bf16"] * FP8_OVER_BF16
@@ -241,7 +241,7 @@ def run_ours(args, rank, world):
 
     cases = []
     for M in Ms:
-        c = make_case(CONFIG_ID, M, device=dev)
+        c = make_case(args.config, M, projection=args.proj, routing=args.routing, device=dev)
         off, *_ = plan_expert_offsets(c.topk_ids, c.E)
         e_act = int(np.count_nonzero(np.diff(off)))
         R = c.R
@@ -353,7 +353,7 @@ def run_ours(args, rank, world):
         roof = dict(bound="hbm", achieved=round(dcs["bytes"] / dg / 1e9, 1),
                     peak=peaks["hbm_gbs"], unit="GB/s")
     roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
-    roof["traffic"] = measured_traffic(dcs["M"])
+    roof["traffic"] = measured_traffic(dcs["M"]) if default_workload(args) else None
     roof["launch"] = f"GEMM at M={dcs['M']} (largest share of the step)"
     roof["peak_source"] = (f"{peaks['source']}: bf16 {peaks['bf16']} TFLOP/s x{FP8_OVER_BF16} "
                            f"nominal fp8/bf16" if roof["bound"] == "tensor"
@@ -426,7 +426,15 @@ def run_ours(args, rank, world):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(Ms[0])
+        cpu = cpu_baseline(Ms[0], args)
+
+    c0 = cases[0]["c"]
+    if default_workload(args):
+        workload, routing_desc = WORKLOAD, "biased (unbalanced)"
+    else:
+        workload = (f"{cfg['name']} {c0.projection} E={c0.E} top{c0.top_k} N={c0.N} K={c0.K} "
+                    f"{c0.routing}, M sweep {Ms[0]}..{Ms[-1]}")
+        routing_desc = c0.routing
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -434,8 +442,8 @@ def run_ours(args, rank, world):
         "ms_per_step": round(dev_max / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 x fp4e2m1 -> f32 acc -> bf16",
         "data": "synthetic (seeded routing, N(0,1) values quantised as the configs state)",
-        "config": {"workload": WORKLOAD, "E": 32, "top_k": 8, "N": 4096, "K": 6144,
-                   "Ms": Ms, "routing": "biased (unbalanced)",
+        "config": {"workload": workload, "E": c0.E, "top_k": c0.top_k, "N": c0.N, "K": c0.K,
+                   "Ms": Ms, "routing": routing_desc,
                    "l2": L2Flush.DESCRIPTION,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "sweep": sweep,
@@ -499,12 +507,19 @@ def time_moe_io(cs, flush, stream, peaks, hg, reps=20):
 
 # ------------------------------------------------------------ oracle arms --
 
-def cpu_baseline(M, budget_s=30.0):
+def default_workload(args):
+    """The workload the headline line is quoted on (configuration 1, gate/up, skewed routing)."""
+    return args.config == CONFIG_ID and args.proj in (None, "gate_up") and \
+        args.routing in (None, "biased")
+
+
+def cpu_baseline(M, args, budget_s=30.0):
     """The CPU oracle as it stands on a bounded sample: plan + full GEMM of M tokens."""
     from oracle import gemm as G
     from oracle.plan import plan_expert_offsets
     from synth import make_case
-    c = make_case(CONFIG_ID, M, device="cpu", cache_weights=False)
+    c = make_case(args.config, M, projection=args.proj, routing=args.routing, device="cpu",
+                  cache_weights=False)
     a, a_s = c.a_fp8.numpy(), c.a_scale.numpy()
     w, w_s = c.w_fp4.numpy(), c.w_scale.numpy()
     t0 = time.perf_counter()
@@ -514,7 +529,7 @@ def cpu_baseline(M, budget_s=30.0):
     flops = 2.0 * c.R * c.N * c.K
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"gate/up M={M} (R={c.R}): plan + full float64 GEMM over all experts, "
+            "sample": f"{c.projection} M={M} (R={c.R}): plan + full float64 GEMM over all experts, "
                       f"{dt:.1f} s; numpy decode single-threaded, matmul on the host BLAS "
                       f"threads ({os.cpu_count()} cores)"}
 
@@ -527,7 +542,8 @@ def run_reference(args, rank, world):
     from oracle.plan import plan_expert_offsets
     from synth import make_case
     M = 64
-    c = make_case(CONFIG_ID, M, device="cpu", cache_weights=False)
+    c = make_case(args.config, M, projection=args.proj, routing=args.routing, device="cpu",
+                  cache_weights=False)
     a, a_s = c.a_fp8.numpy(), c.a_scale.numpy()
     w, w_s = c.w_fp4.numpy(), c.w_scale.numpy()
     # bounded sample per step: the experts of the first 2 tokens' routing
@@ -549,14 +565,16 @@ def run_reference(args, rank, world):
         step()
     dt = time.perf_counter() - t0
     v = flops_step * args.steps / dt / 1e12
-    sample = (f"gate/up M={M}: plan + float64 GEMM of the {len(sel)} experts routed by the first "
-              f"2 tokens ({int(sum(off[e + 1] - off[e] for e in sel))} rows) per step")
+    sample = (f"{c.projection} M={M}: plan + float64 GEMM of the {len(sel)} experts routed by "
+              f"the first 2 tokens ({int(sum(off[e + 1] - off[e] for e in sel))} rows) per step")
+    workload = WORKLOAD if default_workload(args) else (
+        f"config {args.config} {c.projection} E={c.E} top{c.top_k} N={c.N} K={c.K} {c.routing}")
     return {
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "data": "synthetic", "config": {"workload": workload, "sample": sample},
         "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "kind": "oracle",
                          "cores": os.cpu_count(), "sample": sample},
         "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -571,6 +589,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--Ms", type=lambda s: [int(x) for x in s.split(",")], default=None)
+    # another configuration's shapes (for profiling; the headline is configuration 1)
+    ap.add_argument("--config", type=int, default=CONFIG_ID)
+    ap.add_argument("--proj", default=None)
+    ap.add_argument("--routing", default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe-io", action="store_true")
