@@ -23,12 +23,16 @@
 //    tensor core's scale layout (activation scales are per 128-K, replicated
 //    into the four 32-K blocks they cover); warp 1 copies scales to TMEM and
 //    issues tcgen05.mma kind::mxf8f6f4 with block scaling, accumulating FP32
-//    in TMEM; warps 4..7 drain the TMEM accumulator (double-buffered) to BF16
-//    with stores cut at the expert's last row.
-//  * variants (GemmCfg): token tile, ring depth, CTAs per SM; split-K over
-//    clusters of four (partials reduce-scattered through distributed shared
-//    memory); two 128-row weight blocks per unit; and a CTA-pair kernel
-//    (tcgen05 cta_group::2, grouped_w4a8_pair_kernel).
+//    in TMEM; warps 4..7 drain the TMEM accumulator to BF16 with stores cut
+//    at the expert's last row (two accumulator buffers, or one where two
+//    224-row pipelines share an SM's TMEM).
+//  * variants (GemmCfg): token tile, ring depth, CTAs per SM, accumulator
+//    buffers; split-K over clusters of four (partials reduce-scattered
+//    through distributed shared memory); two 128-row weight blocks per unit;
+//    and a CTA-pair kernel (tcgen05 cta_group::2, grouped_w4a8_pair_kernel).
+//    The host picks one from the mean rows per expert, with wave models of
+//    the resident CTAs at the split-K and 112/224-row boundaries
+//    (gemm_pick_variant).
 //  * every barrier wait is bounded (see wait_bounded).
 #include <cuda_bf16.h>
 
