@@ -197,8 +197,9 @@ hg_status hg_grouped_w4a8_gemm_mmajor(const uint8_t* a_fp8, const uint8_t* a_sca
  * an expert with r rows is cut into ceil(r / T) tiles of equal size rounded
  * up to 16 rows.  The choice can depend on the current device's SM count
  * and cluster occupancy, which this asks for when a device is present
- * (without one, the split-K variant is never chosen).  Launches nothing;
- * 0 for invalid arguments.
+ * (without one, the split-K variant is never chosen and the boundary between
+ * the 112- and 224-row tiles stays at 192 rows per expert).  Launches
+ * nothing; 0 for invalid arguments.
  */
 int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows);
 
