@@ -135,3 +135,23 @@ def test_graph_capture_and_replay(cuda_lib):
         out_d, _, _ = _device_calls(cuda_lib, c)
         assert torch.equal(out.view(torch.int16), out_d.view(torch.int16))
     assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def test_dropped_ids(cuda_lib):
+    # ids outside [0, E) are dropped by the plan: the rows before off[E] carry
+    # results equal to the device calls', the count is reported
+    c = make_case(1, 64, projection="gate_up", routing="biased")
+    ids = np.ascontiguousarray(c.topk_ids).copy()
+    ids[::7, 0] = -1
+    ids[3::11, 1] = c.E
+    c.topk_ids = ids
+    cuda_lib.hg_get_device_status()
+    out_h, off_h, s2s_h = _host_call(cuda_lib, c)
+    st, detail = cuda_lib.hg_get_device_status()
+    ref_off, ref_s2s, _, bad = plan_expert_offsets(ids, c.E)
+    assert bad > 0 and st == cuda_lib.HG_ERR_BAD_IDS and detail == bad
+    assert np.array_equal(off_h.numpy(), ref_off) and np.array_equal(s2s_h.numpy(), ref_s2s)
+    out_d, off_d, _ = _device_calls(cuda_lib, c)
+    cuda_lib.hg_get_device_status()
+    n = int(ref_off[-1])
+    assert torch.equal(out_h[:n].view(torch.int16), out_d[:n].view(torch.int16))
