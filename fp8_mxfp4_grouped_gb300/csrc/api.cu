@@ -114,6 +114,16 @@ const char* hg_status_string(int status) {
 
 int hg_version(void) { return 100; }
 
+hg_status hg_shutdown(void) {
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        for (int d = 0; d < kMaxDevices; ++d) g_dev[d] = DeviceInfo{};
+    }
+    gemm_reset_caches();
+    plan_noalloc_reset();
+    return HG_OK;
+}
+
 size_t hg_plan_workspace_bytes(int32_t M, int32_t top_k, int32_t E) {
     if (M < 0 || top_k < 1 || E < 1) return 0;
     const long long R = static_cast<long long>(M) * top_k;

@@ -1091,24 +1091,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) occupancy_stand_in() {}
 // (clusters are placed whole inside a GPC, so this can be below
 // num_sms * ctas_per_sm / cl).  Cached per kernel, device and shared-memory
 // size; 0 when the query fails.
+struct ClusterEntry {
+    const void* fn;
+    int dev;
+    int cl;
+    size_t smem;
+    int value;
+};
+ClusterEntry g_cluster_cache[32];
+int g_cluster_used = 0;
+std::mutex g_cluster_mu;
+
 int resident_clusters(const void* fn, int cl, int threads, size_t smem, bool attr_cluster) {
-    struct Entry {
-        const void* fn;
-        int dev;
-        int cl;
-        size_t smem;
-        int value;
-    };
-    static Entry cache[32];
-    static int used = 0;
-    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i) {
-        if (cache[i].fn == fn && cache[i].dev == dev && cache[i].cl == cl && cache[i].smem == smem) {
-            return cache[i].value;
-        }
+    std::lock_guard<std::mutex> lock(g_cluster_mu);
+    for (int i = 0; i < g_cluster_used; ++i) {
+        const ClusterEntry& c = g_cluster_cache[i];
+        if (c.fn == fn && c.dev == dev && c.cl == cl && c.smem == smem) return c.value;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cl), 1, 1);
@@ -1128,14 +1128,37 @@ int resident_clusters(const void* fn, int cl, int threads, size_t smem, bool att
         cudaGetLastError();
         n = 0;
     }
-    if (used < 32) cache[used++] = Entry{fn, dev, cl, smem, n};
+    if (g_cluster_used < 32) g_cluster_cache[g_cluster_used++] = ClusterEntry{fn, dev, cl, smem, n};
     return n;
 }
 
+// A kernel's dynamic shared-memory limit is a per-device setting: applied
+// once per (kernel, device, size) and remembered until gemm_reset_caches.
+struct AttrEntry {
+    const void* fn;
+    int dev;
+    size_t bytes;
+    cudaError_t err;
+};
+AttrEntry g_attr_cache[64];
+int g_attr_used = 0;
+std::mutex g_attr_mu;
+
 template <class Kern>
 cudaError_t set_smem_attr(Kern* fn, size_t bytes) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(bytes));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const void* key = reinterpret_cast<const void*>(fn);
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    for (int i = 0; i < g_attr_used; ++i) {
+        const AttrEntry& c = g_attr_cache[i];
+        if (c.fn == key && c.dev == dev && c.bytes == bytes) return c.err;
+    }
+    const cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(bytes));
+    if (err != cudaSuccess) cudaGetLastError();
+    if (g_attr_used < 64) g_attr_cache[g_attr_used++] = AttrEntry{key, dev, bytes, err};
+    return err;
 }
 
 // CTAs one launch uses (0: nothing to do).  Persistent grids: C CTAs per SM,
@@ -1153,8 +1176,8 @@ template <class Cfg>
 long long grid_cluster(const GemmArgs& a) {
     constexpr int CL = Cfg::kCluster;
     auto* stand_in = occupancy_stand_in<Cfg::kThreads, Cfg::kCtasPerSm>;
-    static cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
-    static cudaError_t attr_s = set_smem_attr(stand_in, kSmemPerBlockMax);
+    const cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
+    const cudaError_t attr_s = set_smem_attr(stand_in, kSmemPerBlockMax);
     if (attr != cudaSuccess || attr_s != cudaSuccess) return 0;
     long long grid = static_cast<long long>(a.num_sms) * Cfg::kCtasPerSm / CL * CL;
     const int res = resident_clusters(reinterpret_cast<const void*>(stand_in), CL, Cfg::kThreads,
@@ -1167,8 +1190,8 @@ long long grid_cluster(const GemmArgs& a) {
 template <class Cfg>
 long long grid_pair(const GemmArgs& a) {
     auto* stand_in = occupancy_stand_in<Cfg::kThreads, Cfg::kCtasPerSm>;
-    static cudaError_t attr = set_smem_attr(grouped_w4a8_pair_kernel<Cfg>, Cfg::smem_bytes(kMaxE));
-    static cudaError_t attr_s = set_smem_attr(stand_in, kSmemPerBlockMax);
+    const cudaError_t attr = set_smem_attr(grouped_w4a8_pair_kernel<Cfg>, Cfg::smem_bytes(kMaxE));
+    const cudaError_t attr_s = set_smem_attr(stand_in, kSmemPerBlockMax);
     if (attr != cudaSuccess || attr_s != cudaSuccess) return 0;
     long long pairs = static_cast<long long>(a.num_sms / 2) * Cfg::kCtasPerSm;
     const int res = resident_clusters(reinterpret_cast<const void*>(stand_in), 2, Cfg::kThreads,
@@ -1181,7 +1204,7 @@ long long grid_pair(const GemmArgs& a) {
 template <class Cfg>
 cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
                        cudaStream_t stream) {
-    static cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
+    const cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
     if (attr != cudaSuccess) return attr;
     const long long grid = grid_plain<Cfg>(a);
     if (grid < 1) return cudaSuccess;
@@ -1231,6 +1254,15 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const AMaps
 }  // namespace
 
 int gemm_max_experts() { return kMaxE; }
+
+void gemm_reset_caches() {
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        g_attr_used = 0;
+    }
+    std::lock_guard<std::mutex> lock(g_cluster_mu);
+    g_cluster_used = 0;
+}
 
 int gemm_variant_max_experts(int variant) {
     switch (variant) {

@@ -112,6 +112,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, con
 size_t gemm_smem_bytes(int variant, int32_t E);
 long long gemm_launch_ctas(const GemmArgs& a);   // CTAs the launch would use
 int gemm_max_experts();
+// Forget the per-device kernel settings and occupancy answers (hg_shutdown).
+void gemm_reset_caches();
+// Forget the plan scratch array's per-device addresses (hg_shutdown).
+void plan_noalloc_reset();
 int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms);
 int gemm_variant_token_tile(int variant);
 int gemm_variant_max_experts(int variant);

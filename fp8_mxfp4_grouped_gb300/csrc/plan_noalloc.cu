@@ -46,6 +46,12 @@ hg_status scratch_for_current_device(int32_t** out) {
 }
 
 }  // namespace
+
+void plan_noalloc_reset() {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    for (int d = 0; d < kMaxDevices; ++d) g_scratch_ptr[d] = nullptr;
+}
+
 }  // namespace hg
 
 extern "C" hg_status hg_plan_expert_offsets_noalloc(const int32_t* topk_ids, int32_t M,

@@ -31,6 +31,8 @@ lib.hg_status_string.argtypes = [ctypes.c_int]
 lib.hg_status_string.restype = ctypes.c_char_p
 lib.hg_version.argtypes = []
 lib.hg_version.restype = ctypes.c_int
+lib.hg_shutdown.argtypes = []
+lib.hg_shutdown.restype = ctypes.c_int
 lib.hg_plan_workspace_bytes.argtypes = [_i32, _i32, _i32]
 lib.hg_plan_workspace_bytes.restype = _sz
 lib.hg_plan_block_threads.argtypes = [_i32, _i32]
@@ -96,6 +98,11 @@ def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def hg_shutdown() -> None:
+    """Drop the library's per-device caches (see include/hg.h)."""
+    _check(lib.hg_shutdown(), "hg_shutdown")
 
 
 def hg_plan_workspace_bytes(M: int, top_k: int, E: int) -> int:

@@ -53,6 +53,20 @@ const char* hg_status_string(int status);
 /* Library version, major*10000 + minor*100 + patch. */
 int hg_version(void);
 
+/*
+ * Drop the library's per-device state: the cached device properties, the
+ * device addresses of its status word and of the no-allocation plan's
+ * scratch array, the kernels' shared-memory settings and the
+ * cluster-residency answers.  The next call on a device queries them again.
+ * Call it before using the library in a new context on a device whose
+ * context was destroyed (cudaDeviceReset): the cached addresses and settings
+ * belong to the old context.  Frees nothing: the status word and the scratch
+ * array are module variables that live and die with their context, and the
+ * library makes no device allocation of its own.  Must not run concurrently
+ * with other calls of the library.  Host-only; returns HG_OK.
+ */
+hg_status hg_shutdown(void);
+
 /* ---------------------------------------------------------------- plan -- */
 
 /*

@@ -181,3 +181,9 @@ def test_plan_launches_rejects_bad_arguments_without_a_device(lib):
     assert lib.hg_plan_launches(4, 8, 0) == -1
     assert lib.hg_plan_launches(0, 8, 32) == 0
     assert lib.hg_plan_launches(1 << 30, 8, 32) == -1
+
+
+def test_shutdown_without_a_device(lib):
+    # host-only: drops the caches, nothing to free, safe to repeat
+    assert lib.lib.hg_shutdown() == lib.HG_OK
+    assert lib.lib.hg_shutdown() == lib.HG_OK

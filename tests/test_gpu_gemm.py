@@ -395,3 +395,20 @@ def test_mmajor_matches_row_major_full_size(cuda_lib, cid, M):
     torch.cuda.synchronize()
     assert torch.equal(o_row.view(torch.int16), o_mm.view(torch.int16))
     assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def test_shutdown_then_reuse(cuda_lib):
+    # after hg_shutdown every per-device setting is queried and applied again
+    c = make_case(1, 64)
+    ids = torch.from_numpy(c.topk_ids).cuda()
+    args = (c.a_fp8.cuda(), c.a_scale.cuda(), c.w_fp4.cuda(), c.w_scale.cuda())
+    off, _, _ = cuda_lib.hg_plan_expert_offsets(ids, c.E)
+    before = cuda_lib.hg_grouped_w4a8_gemm(*args, off)
+    torch.cuda.synchronize()
+    cuda_lib.hg_shutdown()
+    off2, _, _ = cuda_lib.hg_plan_expert_offsets(ids, c.E)
+    after = cuda_lib.hg_grouped_w4a8_gemm(*args, off2)
+    torch.cuda.synchronize()
+    assert torch.equal(off, off2)
+    assert torch.equal(before.view(torch.int16), after.view(torch.int16))
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
