@@ -412,3 +412,35 @@ def test_shutdown_then_reuse(cuda_lib):
     assert torch.equal(off, off2)
     assert torch.equal(before.view(torch.int16), after.view(torch.int16))
     assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def _random_problem(seed):
+    """A seeded random small problem: expert count, shapes, row counts per
+    expert (some empty, some past a tile boundary), codes and scale range."""
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 41))
+    N = 128 * int(rng.integers(1, 5))
+    K = 512 * int(rng.integers(1, 4))
+    sizes = rng.integers(0, 260, E)
+    sizes[rng.random(E) < 0.25] = 0
+    cuts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    lo = int(rng.integers(110, 128))
+    a, a_s, w, w_s = _rand_codes(rng, int(cuts[-1]), K, E, N, scale_lo=lo, scale_hi=lo + 16)
+    return E, N, K, cuts, a, a_s, w, w_s
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_problems_every_variant(cuda_lib, seed):
+    # one oracle result per problem, compared with every variant and with the
+    # automatic choice
+    E, N, K, cuts, a, a_s, w, w_s = _random_problem(9000 + seed)
+    ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K)
+    prev = cuda_lib.hg_set_gemm_variant(0)
+    try:
+        for v in [0] + VARIANTS:
+            cuda_lib.hg_set_gemm_variant(v)
+            out = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
+            assert_rows_close(bf16_bits(out), ref, f"seed {seed} variant {v} E={E} N={N} K={K}")
+    finally:
+        cuda_lib.hg_set_gemm_variant(prev)
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
