@@ -114,3 +114,23 @@ def test_plan_launch_count(cuda_lib):
     assert cuda_lib.hg_plan_launches(4097, 8, 32) == 2
     assert cuda_lib.hg_plan_launches(1000, 8, 3000) == 2        # count tables beyond one CTA
     assert cuda_lib.hg_plan_launches(-1, 8, 32) == -1
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_plan_random_problems(cuda_lib, seed):
+    # seeded random sizes across the one-cluster and two-launch paths, some
+    # ids out of range; bit-exact against the oracle
+    rng = np.random.default_rng(5000 + seed)
+    E = int(rng.choice([1, 3, 12, 32, 64, 200, 2000]))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    M = int(rng.choice([1, 7, 100, 513, 4096, 9000, 20000]))
+    ids = rng.integers(0, E, (M, k)).astype(np.int32)
+    if seed % 3 == 0:
+        drop = rng.random((M, k)) < 0.05
+        ids[drop] = rng.choice([-1, E, E + 5], int(drop.sum()))
+    cuda_lib.hg_get_device_status()
+    off, s2d, d2s = _gpu_plan(cuda_lib, ids, E)
+    r_off, r_s2d, r_d2s, bad = plan_expert_offsets(ids, E)
+    assert np.array_equal(off, r_off) and np.array_equal(s2d, r_s2d) and np.array_equal(d2s, r_d2s)
+    st, detail = cuda_lib.hg_get_device_status()
+    assert (st, detail) == ((cuda_lib.HG_ERR_BAD_IDS, bad) if bad else (cuda_lib.HG_OK, 0))
