@@ -127,3 +127,32 @@ def test_moe_layer_end_to_end(cuda_lib):
     ry = G.grouped_w4a8_gemm(ra, rs, w_fp4.numpy(), w_scale.numpy(), off, E, N, K)
     ref = Q.combine_topk(ry, d2s, wts)
     assert_rows_close(bf16_bits(out), ref, "MoE layer")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_problems(cuda_lib, seed):
+    # seeded random sizes: both quantisers bit-exact against the oracle (and
+    # equal to each other), the combine within the GEMM tolerance
+    rng = np.random.default_rng(7000 + seed)
+    E = int(rng.integers(1, 65))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    M = int(rng.integers(1, 401))
+    K = 128 * int(rng.integers(1, 17))
+    N = 128 * int(rng.integers(1, 33))
+    x = _tokens(rng, M, K, special=(seed % 4 == 0 and M >= 6 and K >= 384))
+    ids = make_routing(M, E, k, "biased" if seed % 2 else "uniform", 300 + seed)
+    _, s2d, d2s, _ = plan_expert_offsets(ids, E)
+    xs = x.view(torch.int16).numpy().view(np.uint16)
+    a, s = cuda_lib.hg_quantize_scatter_acts(x.cuda(), k, torch.from_numpy(d2s).cuda())
+    ga, gs = cuda_lib.hg_quantize_gather_acts(x.cuda(), k, torch.from_numpy(s2d).cuda())
+    torch.cuda.synchronize()
+    ra, rs = Q.quantize_scatter(xs, k, d2s)
+    assert np.array_equal(a.cpu().numpy(), ra) and np.array_equal(s.cpu().numpy(), rs)
+    assert torch.equal(a, ga) and torch.equal(s, gs)
+    y = torch.from_numpy(rng.standard_normal((M * k, N)).astype(np.float32)).to(torch.bfloat16)
+    w = rng.random((M, k)).astype(np.float32)
+    out = cuda_lib.hg_combine_topk(y.cuda(), torch.from_numpy(d2s).cuda(),
+                                   torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    ref = Q.combine_topk(y.view(torch.int16).numpy().view(np.uint16), d2s, w)
+    assert_rows_close(bf16_bits(out), ref, f"combine seed {seed} M={M} k={k} N={N}")
