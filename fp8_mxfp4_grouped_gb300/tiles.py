@@ -36,7 +36,7 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     one token tile per active expert, it leaves the busiest CTA at least 15 %
     fewer stages than variant 1.  Above 48 rows per expert the default
     (variant 2 up to 192 rows, variant 8 above) moves when a wave model with
-    every expert at the mean predicts a 15 % gain for the other."""
+    every expert at the mean predicts a 14-15 % gain for the other."""
     per = rows // max(E, 1)
     if per <= 48:
         if num_sms > 0 and rows <= 32 * E and K >= 512 and N >= W_TILE and split_ctas >= SPLIT_CLUSTER:
@@ -55,7 +55,7 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
         return default
     # wave model with every expert at the mean; a variant-8 round costs
     # 1.25 + 0.0026 * tile rows variant-2 rounds; moves the default only
-    # for a predicted 15 % gain
+    # for a predicted 14 % gain (to variant 8) or 15 % (to variant 2)
     g = 2 * num_sms
     blocks = E * (N // W_TILE)
     t2 = -(-per // VARIANT_T_MAX[2])
@@ -64,7 +64,7 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     c2 = -(-(blocks * t2) // g) * 10000
     c8 = -(-(blocks * t8) // g) * (12500 + 26 * rows8)
     if default == 2:
-        return 8 if 100 * c8 <= 85 * c2 else 2
+        return 8 if 100 * c8 <= 86 * c2 else 2
     return 2 if 100 * c8 >= 118 * c2 else 8
 
 

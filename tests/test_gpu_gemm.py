@@ -251,7 +251,8 @@ def test_split_k_auto_choice(cuda_lib):
                           (12, 3584, 3072, 32), (32, 4096, 6144, 512), (4, 256, 512, 32),
                           (12, 6144, 3584, 512), (32, 4096, 6144, 16384),
                           (12, 6144, 3584, 1408), (12, 6144, 3584, 1792), (12, 3584, 3072, 2560),
-                          (12, 3584, 3072, 3072), (32, 6144, 2048, 4096), (32, 4096, 6144, 9216)]:
+                          (12, 3584, 3072, 3072), (32, 6144, 2048, 4096), (32, 4096, 6144, 9216),
+                          (12, 6144, 3584, 2048)]:
         v = T.pick_variant(E, N, rows, K, sms, split_ctas)
         assert cuda_lib.hg_gemm_token_tile(E, N, K, rows) == T.VARIANT_T_MAX[v], (E, N, K, rows)
     assert T.pick_variant(12, 6144, 8, 3584, sms, split_ctas) == 6
