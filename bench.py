@@ -123,6 +123,119 @@ def host_link_gbs(cs, dev):
                 both=round((nu + nd) / tb / 1e9, 1))
 
 
+def device_buffers(c, dev, hg):
+    """Device-side ids, plan outputs, plan workspace and GEMM output of one case."""
+    R = c.R
+    return dict(
+        ids=torch.from_numpy(c.topk_ids).to(dev),
+        off=torch.empty(c.E + 1, dtype=torch.int32, device=dev),
+        s2d=torch.empty(R, dtype=torch.int32, device=dev),
+        d2s=torch.empty(R, dtype=torch.int32, device=dev),
+        ws=torch.empty(max(4, hg.hg_plan_workspace_bytes(c.M, c.top_k, c.E)),
+                       dtype=torch.uint8, device=dev),
+        out=torch.empty((R, c.N), dtype=torch.bfloat16, device=dev),
+    )
+
+
+def active_experts(bufs, c, stream, hg):
+    """Experts with at least one row, counted from the GPU plan's offsets
+    (untimed bookkeeping for the roofline's weight bytes)."""
+    hg.hg_plan_expert_offsets(bufs["ids"], c.E, bufs["off"], bufs["s2d"], bufs["d2s"], bufs["ws"],
+                              stream=stream)
+    stream.synchronize()
+    return int(np.count_nonzero(np.diff(bufs["off"].cpu().numpy())))
+
+
+def sweep_entry(cs, g_us, p_us, peaks, fp8_peak):
+    """One measured launch against its roofline: roof_frac = max(HBM time, FP8 tensor
+    time) / measured time; hbm_frac = algorithmic bytes / time / HBM peak."""
+    t_hbm = cs["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = cs["flops"] / (fp8_peak * 1e12)
+    return dict(M=cs["M"], R=cs["R"], E_act=cs["e_act"], gemm_us=round(g_us, 2),
+                plan_us=round(p_us, 2), tflops=round(cs["flops"] / g_us / 1e6, 1),
+                gbs=round(cs["bytes"] / g_us / 1e3, 1),
+                bound="hbm" if t_hbm >= t_tc else "tensor",
+                roof_frac=round(max(t_hbm, t_tc) / (g_us * 1e-6), 3),
+                hbm_frac=round(t_hbm / (g_us * 1e-6), 3))
+
+
+# The other workloads' shapes, each measured like the headline sweep (plan,
+# then GEMM, L2 flushed before every pair) and reported beside it.
+OTHER_WORKLOADS = [(2, "down", "biased"), (3, "w13", "uniform"), (3, "w2", "uniform"),
+                   (4, "gate_up", "uniform"), (4, "gate_up", "biased"),
+                   (4, "down", "uniform"), (4, "down", "biased")]
+
+
+def time_other_workloads(flush, stream, peaks, fp8_peak, hg, reps, warm=3):
+    """Median plan and GEMM device time of every M of the other workloads."""
+    from synth import make_case
+    from synth.inputs import CONFIGS
+    dev = torch.device("cuda")
+    out = []
+    for cid, proj, routing in OTHER_WORKLOADS:
+        rows = []
+        c = None
+        for M in CONFIGS[cid]["Ms"]:
+            c = make_case(cid, M, projection=proj, routing=routing, device=dev)
+            b = device_buffers(c, dev, hg)
+            e_act = active_experts(b, c, stream, hg)
+            flops, byts = algorithmic(c.R, e_act, c.E, c.N, c.K)
+            evs = []
+            for it in range(warm + reps):
+                with torch.cuda.stream(stream):
+                    flush(it)
+                    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                    e[0].record(stream)
+                    hg.hg_plan_expert_offsets(b["ids"], c.E, b["off"], b["s2d"], b["d2s"],
+                                              b["ws"], stream=stream)
+                    e[1].record(stream)
+                    hg.hg_grouped_w4a8_gemm(c.a_fp8, c.a_scale, c.w_fp4, c.w_scale, b["off"],
+                                            out=b["out"], stream=stream)
+                    e[2].record(stream)
+                if it >= warm:
+                    evs.append(e)
+            torch.cuda.synchronize()
+            p = statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in evs)
+            g = statistics.median(e[1].elapsed_time(e[2]) * 1e3 for e in evs)
+            cs = dict(M=M, R=c.R, e_act=e_act, flops=flops, bytes=byts)
+            entry = sweep_entry(cs, g, p, peaks, fp8_peak)
+            entry["variant_token_tile"] = hg.hg_gemm_token_tile(c.E, c.N, c.K, c.R)
+            rows.append(entry)
+            del b
+        out.append(dict(config=cid, projection=proj, routing=routing, E=c.E, top_k=c.top_k,
+                        N=c.N, K=c.K, reps=reps, sweep=rows))
+        del c
+        torch.cuda.empty_cache()
+    st, detail = hg.hg_get_device_status()
+    if st != hg.HG_OK:
+        raise RuntimeError(f"device status {st} detail {detail} after the other workloads")
+    return out
+
+
+def target_summary(headline_sweep, others):
+    """The two throughput targets over every measured shape: the lowest roofline
+    fraction at M >= 4096, and the lowest HBM-roofline fraction at M <= 256."""
+    rows = [("config1 gate_up biased", r) for r in headline_sweep]
+    for w in others:
+        rows += [(f"config{w['config']} {w['projection']} {w['routing']}", r) for r in w["sweep"]]
+    big = [(n, r) for n, r in rows if r["M"] >= 4096]
+    small = [(n, r) for n, r in rows if r["M"] <= 256]
+    out = {}
+    if big:
+        n, r = min(big, key=lambda x: x[1]["roof_frac"])
+        out["m_ge_4096_min_roof_frac"] = dict(value=r["roof_frac"], at=f"{n} M={r['M']}",
+                                              target=0.70,
+                                              below=[f"{a} M={b['M']}: {b['roof_frac']}"
+                                                     for a, b in big if b["roof_frac"] < 0.70])
+    if small:
+        n, r = min(small, key=lambda x: x[1]["hbm_frac"])
+        out["m_le_256_min_hbm_frac"] = dict(value=r["hbm_frac"], at=f"{n} M={r['M']}",
+                                            target=0.50,
+                                            below=[f"{a} M={b['M']}: {b['hbm_frac']}"
+                                                   for a, b in small if b["hbm_frac"] < 0.50])
+    return out
+
+
 def algorithmic(R, E_act, E, N, K):
     """GEMM flops and the bytes each operand must cross HBM once."""
     flops = 2.0 * R * N * K
@@ -226,7 +339,6 @@ class ClockSampler:
 
 def run_ours(args, rank, world):
     from fp8_mxfp4_grouped_gb300 import hg
-    from oracle.plan import plan_expert_offsets  # bookkeeping only (E_act), not timed
     from synth import make_case
     from synth.inputs import CONFIGS
 
@@ -242,19 +354,9 @@ def run_ours(args, rank, world):
     cases = []
     for M in Ms:
         c = make_case(args.config, M, projection=args.proj, routing=args.routing, device=dev)
-        off, *_ = plan_expert_offsets(c.topk_ids, c.E)
-        e_act = int(np.count_nonzero(np.diff(off)))
         R = c.R
-        ids = torch.from_numpy(c.topk_ids).to(dev)
-        bufs = dict(
-            ids=ids,
-            off=torch.empty(c.E + 1, dtype=torch.int32, device=dev),
-            s2d=torch.empty(R, dtype=torch.int32, device=dev),
-            d2s=torch.empty(R, dtype=torch.int32, device=dev),
-            ws=torch.empty(max(4, hg.hg_plan_workspace_bytes(M, c.top_k, c.E)),
-                           dtype=torch.uint8, device=dev),
-            out=torch.empty((R, c.N), dtype=torch.bfloat16, device=dev),
-        )
+        bufs = device_buffers(c, dev, hg)
+        e_act = active_experts(bufs, c, stream, hg)
         # pinned host copies for the end-to-end leg
         host = dict(ids=torch.from_numpy(c.topk_ids).pin_memory(),
                     a=c.a_fp8.cpu().pin_memory(), a_s=c.a_scale.cpu().pin_memory(),
@@ -332,17 +434,8 @@ def run_ours(args, rank, world):
     flops_all = reduce_scalar(flops_step * args.steps, "sum", world)
     value = flops_all / dev_max / 1e12
 
-    sweep = []
-    for i, cs in enumerate(cases):
-        g = statistics.median(gemm_us[i])
-        p = statistics.median(plan_us[i])
-        t_hbm = cs["bytes"] / (peaks["hbm_gbs"] * 1e9)
-        t_tc = cs["flops"] / (fp8_peak * 1e12)
-        bound = "hbm" if t_hbm >= t_tc else "tensor"
-        sweep.append(dict(M=cs["M"], R=cs["R"], E_act=cs["e_act"], gemm_us=round(g, 2),
-                          plan_us=round(p, 2), tflops=round(cs["flops"] / g / 1e6, 1),
-                          gbs=round(cs["bytes"] / g / 1e3, 1), bound=bound,
-                          roof_frac=round(max(t_hbm, t_tc) / (g * 1e-6), 3)))
+    sweep = [sweep_entry(cs, statistics.median(gemm_us[i]), statistics.median(plan_us[i]),
+                         peaks, fp8_peak) for i, cs in enumerate(cases)]
     dom = max(range(len(cases)), key=lambda i: statistics.median(gemm_us[i]))
     dcs = cases[dom]
     dg = statistics.median(gemm_us[dom]) * 1e-6
@@ -424,17 +517,15 @@ def run_ours(args, rank, world):
 
     moe_io = None if args.no_moe_io else time_moe_io(cases[-1], flush, stream, peaks, hg)
 
+    others = None
+    if default_workload(args) and not args.no_other_workloads:
+        others = time_other_workloads(flush, stream, peaks, fp8_peak, hg,
+                                      reps=max(5, min(args.steps, 20)))
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(Ms[0], args)
+        cpu = cpu_baseline(args)
 
-    c0 = cases[0]["c"]
-    if default_workload(args):
-        workload, routing_desc = WORKLOAD, "biased (unbalanced)"
-    else:
-        workload = (f"{cfg['name']} {c0.projection} E={c0.E} top{c0.top_k} N={c0.N} K={c0.K} "
-                    f"{c0.routing}, M sweep {Ms[0]}..{Ms[-1]}")
-        routing_desc = c0.routing
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -442,11 +533,10 @@ def run_ours(args, rank, world):
         "ms_per_step": round(dev_max / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 x fp4e2m1 -> f32 acc -> bf16",
         "data": "synthetic (seeded routing, N(0,1) values quantised as the configs state)",
-        "config": {"workload": workload, "E": c0.E, "top_k": c0.top_k, "N": c0.N, "K": c0.K,
-                   "Ms": Ms, "routing": routing_desc,
-                   "l2": L2Flush.DESCRIPTION,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": line_config(args, world),
         "sweep": sweep,
+        "other_workloads": others,
+        "targets": target_summary(sweep, others or []),
         "roofline": roof,
         "moe_io": moe_io,
         "cpu_baseline": cpu,
@@ -513,70 +603,92 @@ def default_workload(args):
         args.routing in (None, "biased")
 
 
-def cpu_baseline(M, args, budget_s=30.0):
-    """The CPU oracle as it stands on a bounded sample: plan + full GEMM of M tokens."""
-    from oracle import gemm as G
-    from oracle.plan import plan_expert_offsets
-    from synth import make_case
-    c = make_case(args.config, M, projection=args.proj, routing=args.routing, device="cpu",
-                  cache_weights=False)
-    a, a_s = c.a_fp8.numpy(), c.a_scale.numpy()
-    w, w_s = c.w_fp4.numpy(), c.w_scale.numpy()
-    t0 = time.perf_counter()
-    off, *_ = plan_expert_offsets(c.topk_ids, c.E)
-    G.grouped_w4a8_gemm(a, a_s, w, w_s, off, c.E, c.N, c.K)
-    dt = time.perf_counter() - t0
-    flops = 2.0 * c.R * c.N * c.K
-    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{c.projection} M={M} (R={c.R}): plan + full float64 GEMM over all experts, "
-                      f"{dt:.1f} s; numpy decode single-threaded, matmul on the host BLAS "
-                      f"threads ({os.cpu_count()} cores)"}
+def line_config(args, world):
+    """The `config` object both arms print: the workload, its shapes and the L2 rule."""
+    from synth.inputs import CONFIGS
+    cfg = CONFIGS[args.config]
+    Ms = args.Ms or cfg["Ms"]
+    proj = args.proj or list(cfg["proj"])[0]
+    routing = args.routing or cfg["routing"][0]
+    N, K = cfg["proj"][proj]
+    if default_workload(args):
+        workload, routing_desc = WORKLOAD, "biased (unbalanced)"
+    else:
+        workload = (f"{cfg['name']} {proj} E={cfg['E']} top{cfg['top_k']} N={N} K={K} "
+                    f"{routing}, M sweep {Ms[0]}..{Ms[-1]}")
+        routing_desc = routing
+    return {"workload": workload, "E": cfg["E"], "top_k": cfg["top_k"], "N": N, "K": K,
+            "Ms": Ms, "routing": routing_desc, "l2": L2Flush.DESCRIPTION,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+class OracleSample:
+    """The CPU oracle as it stands, on a bounded sample of the workload: the
+    routing plan and the full float64 GEMM (every expert) of the sweep's
+    smallest M.  Both the cpu_baseline leg and the --impl reference arm time
+    exactly this."""
+
+    def __init__(self, args):
+        from synth import make_case
+        from synth.inputs import CONFIGS
+        M = (args.Ms or CONFIGS[args.config]["Ms"])[0]
+        c = make_case(args.config, M, projection=args.proj, routing=args.routing, device="cpu",
+                      cache_weights=False)
+        self.c = c
+        self.a, self.a_s = c.a_fp8.numpy(), c.a_scale.numpy()
+        self.w, self.w_s = c.w_fp4.numpy(), c.w_scale.numpy()
+        self.flops = 2.0 * c.R * c.N * c.K
+        self.desc = (f"{c.projection} M={M} (R={c.R}): oracle plan + full float64 GEMM over all "
+                     f"{c.E} experts per step; numpy decode single-threaded, matmul on the host "
+                     f"BLAS threads ({os.cpu_count()} cores)")
+
+    def step(self):
+        from oracle import gemm as G
+        from oracle.plan import plan_expert_offsets
+        c = self.c
+        off, *_ = plan_expert_offsets(c.topk_ids, c.E)
+        G.grouped_w4a8_gemm(self.a, self.a_s, self.w, self.w_s, off, c.E, c.N, c.K)
+
+
+def cpu_baseline(args):
+    """The oracle sample timed on the host cores: the median of 3 reps when one
+    rep takes under 10 s, else that one rep."""
+    smp = OracleSample(args)
+    ts = []
+    while len(ts) < 3:
+        t0 = time.perf_counter()
+        smp.step()
+        ts.append(time.perf_counter() - t0)
+        if ts[0] >= 10.0:
+            break
+    dt = statistics.median(ts)
+    return {"value": round(smp.flops / dt / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle", "reps": len(ts), "s_per_rep": round(dt, 2),
+            "sample": smp.desc}
 
 
 def run_reference(args, rank, world):
-    """--impl reference: the CPU oracle timed on the host cores (rank 0 only)."""
+    """--impl reference: the oracle sample timed on the host cores (rank 0 only),
+    W untimed steps then K timed ones."""
     if rank != 0:
         return None
-    from oracle import gemm as G
-    from oracle.plan import plan_expert_offsets
-    from synth import make_case
-    M = 64
-    c = make_case(args.config, M, projection=args.proj, routing=args.routing, device="cpu",
-                  cache_weights=False)
-    a, a_s = c.a_fp8.numpy(), c.a_scale.numpy()
-    w, w_s = c.w_fp4.numpy(), c.w_scale.numpy()
-    # bounded sample per step: the experts of the first 2 tokens' routing
-    off, *_ = plan_expert_offsets(c.topk_ids, c.E)
-    sel = sorted(set(int(x) for x in c.topk_ids[:2].ravel()))
-    flops_step = sum(2.0 * (off[e + 1] - off[e]) * c.N * c.K for e in sel)
-
-    def step():
-        o, *_ = plan_expert_offsets(c.topk_ids, c.E)
-        for e in sel:
-            lo, hi = int(o[e]), int(o[e + 1])
-            sub = np.array([0, hi - lo], dtype=np.int64)
-            G.grouped_w4a8_gemm(a[lo:hi], a_s[lo:hi], w[e:e + 1], w_s[e:e + 1], sub, 1, c.N, c.K)
-
+    smp = OracleSample(args)
     for _ in range(args.warmup):
-        step()
+        smp.step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        smp.step()
     dt = time.perf_counter() - t0
-    v = flops_step * args.steps / dt / 1e12
-    sample = (f"{c.projection} M={M}: plan + float64 GEMM of the {len(sel)} experts routed by "
-              f"the first 2 tokens ({int(sum(off[e + 1] - off[e] for e in sel))} rows) per step")
-    workload = WORKLOAD if default_workload(args) else (
-        f"config {args.config} {c.projection} E={c.E} top{c.top_k} N={c.N} K={c.K} {c.routing}")
+    v = smp.flops * args.steps / dt / 1e12
     return {
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": workload, "sample": sample},
+        "data": "synthetic (seeded routing, N(0,1) values quantised as the configs state)",
+        "config": line_config(args, world),
         "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "kind": "oracle",
-                         "cores": os.cpu_count(), "sample": sample},
+                         "cores": os.cpu_count(), "sample": smp.desc},
         "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -596,6 +708,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe-io", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

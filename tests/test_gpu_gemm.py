@@ -288,9 +288,14 @@ def _sample_rows(off, rng, t_max, per_expert=3, max_experts=6):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-FULL_CASES = [(1, 64, None, None), (1, 768, None, None), (1, 2048, None, None), (2, 64, None, None),
-              (2, 16384, None, None), (3, 1, "w13", None), (3, 256, "w2", None),
-              (4, 4096, "gate_up", "uniform"), (4, 4096, "down", "biased")]
+# Every (configuration, projection, routing, M) of the five workloads except
+# the tiny one (whose full output is compared above), grouped so that each
+# projection's weights are drawn once.
+FULL_CASES = [(cid, M, proj, routing)
+              for cid in (1, 2, 3, 4)
+              for proj in CONFIGS[cid]["proj"]
+              for routing in CONFIGS[cid]["routing"]
+              for M in CONFIGS[cid]["Ms"]]
 
 
 @pytest.mark.parametrize("cid,M,proj,routing", FULL_CASES)
