@@ -4,13 +4,12 @@
 // hg_plan_expert_offsets needs a device workspace for its two-launch path
 // (more than 32768 routed rows, or many experts): one count per block per
 // expert.  Some callers cannot provide one, because they cannot call
-// cudaMalloc at the point where they plan: code that runs while a CUDA graph
-// is being captured (an allocation is not a stream operation, so it cannot be
-// part of the graph), hosts that own every device allocation and do not let
-// a library make its own (framework plugins with a planned memory pool), and
-// latency-critical loops where cudaMalloc's implicit device synchronisation
-// is not acceptable.  hg_plan_expert_offsets_noalloc serves them: its
-// workspace is a fixed-size array in this library's device memory.
+// cudaMalloc at the point where they plan: a host framework that owns every
+// device allocation through its own memory pool and does not let a library
+// allocate behind its back, or a latency-critical loop that cannot take the
+// device-wide synchronisation cudaMalloc and cudaFree may imply.
+// hg_plan_expert_offsets_noalloc serves them: its workspace is a fixed-size
+// array in this library's device memory.
 #include <mutex>
 
 #include "hg_internal.cuh"
