@@ -84,6 +84,100 @@ hg_status encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Tensor-map cache.  A tensor map depends only on its base address and
+// shape, so one encoded for (pointer, sizes) stays valid for any allocation
+// at that address with those sizes; the last few of each kind are kept so
+// that repeated calls on resident buffers skip the five encodes.
+constexpr int kMapCacheEntries = 16;
+struct WMapEntry {
+    const void* p = nullptr;
+    int32_t E = 0, N = 0, K = 0;
+    CUtensorMap map;
+};
+struct AMapEntry {
+    const void* p = nullptr;
+    int32_t rows = 0, K = 0;
+    AMaps maps;
+};
+WMapEntry g_wmap[kMapCacheEntries];
+AMapEntry g_amap[kMapCacheEntries];
+int g_wmap_next = 0;
+int g_amap_next = 0;
+std::mutex g_map_mu;
+
+void map_cache_reset() {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < kMapCacheEntries; ++i) {
+        g_wmap[i].p = nullptr;
+        g_amap[i].p = nullptr;
+    }
+    g_wmap_next = g_amap_next = 0;
+}
+
+// Weights: [E*N rows, K elements] of E2M1, unpacked by the TMA into one
+// 16-byte chunk (8 data bytes + 8 pad) per 16 elements, 128-byte swizzle,
+// boxes of 128 x 128.
+hg_status weight_map(PFN_cuTensorMapEncodeTiled_v12000 encode, const uint8_t* w_fp4, int32_t E,
+                     int32_t N, int32_t K, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < kMapCacheEntries; ++i) {
+        const WMapEntry& c = g_wmap[i];
+        if (c.p == w_fp4 && c.E == E && c.N == N && c.K == K) {
+            *out = c.map;
+            return HG_OK;
+        }
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K),
+                          static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(out, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(w_fp4), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return HG_ERR_CUDA;
+    WMapEntry& slot = g_wmap[g_wmap_next];
+    g_wmap_next = (g_wmap_next + 1) % kMapCacheEntries;
+    slot.p = w_fp4;
+    slot.E = E;
+    slot.N = N;
+    slot.K = K;
+    slot.map = *out;
+    return HG_OK;
+}
+
+// Activations: [rows, K] bytes, 128-byte swizzle; boxes of 16, 32, 64 and
+// 128 rows of 128 bytes.
+hg_status act_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, const uint8_t* a_fp8, int32_t rows,
+                   int32_t K, AMaps* out) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < kMapCacheEntries; ++i) {
+        const AMapEntry& c = g_amap[i];
+        if (c.p == a_fp8 && c.rows == rows && c.K == K) {
+            *out = c.maps;
+            return HG_OK;
+        }
+    }
+    for (int which = 0; which < 4; ++which) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+        cuuint32_t box[2] = {128, 16u << which};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&out->box[which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a_fp8),
+                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return HG_ERR_CUDA;
+    }
+    AMapEntry& slot = g_amap[g_amap_next];
+    g_amap_next = (g_amap_next + 1) % kMapCacheEntries;
+    slot.p = a_fp8;
+    slot.rows = rows;
+    slot.K = K;
+    slot.maps = *out;
+    return HG_OK;
+}
+
 int plan_nblk(long long R) {
     long long n = (R + kPlanIdsPerBlock - 1) / kPlanIdsPerBlock;
     if (n < 1) n = 1;
@@ -121,6 +215,7 @@ hg_status hg_shutdown(void) {
     }
     gemm_reset_caches();
     plan_noalloc_reset();
+    map_cache_reset();
     return HG_OK;
 }
 
@@ -205,7 +300,7 @@ hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scal
     if (E < 1 || N < 1 || K < 1 || rows < 0) return HG_ERR_INVALID_ARG;
     if (!w_fp4 || !w_scale || !expert_offsets) return HG_ERR_INVALID_ARG;
     if (rows > 0 && (!a_fp8 || !a_scale || !out_bf16)) return HG_ERR_INVALID_ARG;
-    if (E > gemm_max_experts() || N % 128 != 0 || K % 512 != 0) return HG_ERR_UNSUPPORTED_SHAPE;
+    if (E > gemm_max_experts() || N % 128 != 0 || K % 128 != 0) return HG_ERR_UNSUPPORTED_SHAPE;
     if (static_cast<long long>(E) * N > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(w_fp4, 32) || !aligned(w_scale, 4)) return HG_ERR_INVALID_ARG;
     if (rows > 0 && (!aligned(a_fp8, 16) || !aligned(out_bf16, 2))) return HG_ERR_INVALID_ARG;
@@ -220,36 +315,12 @@ hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scal
     st = encoder(&encode);
     if (st != HG_OK) return st;
 
-    // Weights: [E*N rows, K elements] of E2M1, unpacked by the TMA into one
-    // 16-byte chunk (8 data bytes + 8 pad) per 16 elements, 128-byte swizzle.
     CUtensorMap map_w;
     AMaps map_a;
-    {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K),
-                              static_cast<cuuint64_t>(E) * static_cast<cuuint64_t>(N)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-        cuuint32_t box[2] = {128, 128};
-        cuuint32_t estr[2] = {1, 1};
-        if (encode(&map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(w_fp4),
-                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return HG_ERR_CUDA;
-    }
-    // Activations: [rows, K] bytes, 128-byte swizzle; boxes of 16, 32, 64 and
-    // 128 rows.
-    for (int which = 0; which < 4; ++which) {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-        cuuint32_t box[2] = {128, 16u << which};
-        cuuint32_t estr[2] = {1, 1};
-        if (encode(&map_a.box[which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                   const_cast<uint8_t*>(a_fp8), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return HG_ERR_CUDA;
-    }
+    st = weight_map(encode, w_fp4, E, N, K, &map_w);
+    if (st != HG_OK) return st;
+    st = act_maps(encode, a_fp8, rows, K, &map_a);
+    if (st != HG_OK) return st;
     GemmArgs a;
     a.a_fp8 = a_fp8;
     a.a_scale = a_scale;
@@ -388,7 +459,7 @@ int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows) {
 }
 
 int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows) {
-    if (E < 1 || E > gemm_max_experts() || N < 128 || N % 128 != 0 || K < 512 || K % 512 != 0 ||
+    if (E < 1 || E > gemm_max_experts() || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0 ||
         rows < 0)
         return 0;
     DeviceInfo* d = nullptr;

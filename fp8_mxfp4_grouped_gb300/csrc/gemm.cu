@@ -173,12 +173,14 @@ using CfgDual = GemmCfg<112, 4, 1, 1, 2>;   // 256 weight rows per unit, one tok
 using CfgWide2 = GemmCfg<224, 2, 2, 1, 1, 1>;   // 224-row tiles, two CTAs per SM, one TMEM buffer each
 
 // Split-K factor for a launch of G CTAs (a multiple of max_split) over U
-// units of KT stages: the s in {1, 2, 4} that minimises the stages of the
-// busiest CTA, ceil(U / (G / s)) * KT / s; ties keep the smaller split.
+// units of KT stages: the s in {1, 2, 4} dividing KT that minimises the
+// stages of the busiest CTA, ceil(U / (G / s)) * KT / s; ties keep the
+// smaller split.
 __host__ __device__ __forceinline__ int choose_split(int U, int KT, int G, int max_split) {
     int best = 1;
     long long best_cost = static_cast<long long>((U + G - 1) / G) * KT;
     for (int s = 2; s <= max_split; s <<= 1) {
+        if (KT % s != 0) continue;
         const int groups = G / s;
         const long long c = static_cast<long long>((U + groups - 1) / groups) * (KT / s);
         if (c < best_cost) {
@@ -253,7 +255,8 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64
 // `row`, K offset `k`, into the swizzled tile at `dst`: one TMA per set bit
 // of n / 16, largest box first, so a tile takes at most four instructions.
 // kPair: the CTA-pair form, `bar` a shared::cluster address in either CTA.
-template <bool kPair = false>
+// kElect: called by a whole converged warp, issued by its elected lane.
+template <bool kPair = false, bool kElect = false>
 __device__ __forceinline__ void load_a_rows(const AMaps& maps, uint32_t dst, int k, int row, int n,
                                             uint32_t bar, uint64_t policy) {
     int r = 0;
@@ -263,6 +266,8 @@ __device__ __forceinline__ void load_a_rows(const AMaps& maps, uint32_t dst, int
         if (n & h) {
             if (kPair) {
                 ptx::tma_load_2d_pair(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
+            } else if (kElect) {
+                ptx::tma_load_2d_elect(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
             } else {
                 ptx::tma_load_2d(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
             }
@@ -404,103 +409,110 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
-        if (lane == 0) {
-            const uint64_t pol_w = ptx::policy_evict_last();   // weight tiles are re-read by the other token tiles of their expert
-            const uint64_t pol_a = ptx::policy_evict_last();
-            uint32_t g = 0;
-            bool ok = true;
-            for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
-                 u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x)) {
-                const Unit t = decode_unit(sch, u);
-                const int wrow = t.e * N + t.n0;
-                for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
-                    const uint32_t slot = g % kStages;
-                    const uint32_t ph = (g / kStages) & 1u;
-                    if (!wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleProducer, slot)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = bar_full_tma + 8 * slot;
-                    ptx::mbar_arrive_expect_tx(fb, Cfg::kMB * kWTileTx + t.n_mma * kBK);
-#pragma unroll
-                    for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                        ptx::tma_load_2d(sbase + Cfg::kOffW + (slot * Cfg::kMB + mb) * kWTileBytes,
-                                         &map_w, ks * kBK, wrow + mb * kBW, fb, pol_w);
-                    }
-                    load_a_rows(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes, ks * kBK,
-                                t.row0, t.n_mma, fb, pol_a);
+        // Like the MMA issuer: the whole warp walks the loop, the elected
+        // lane issues, waits are agreed on with a vote.
+        const uint64_t pol_w = ptx::policy_evict_last();   // weight tiles are re-read by the other token tiles of their expert
+        const uint64_t pol_a = ptx::policy_evict_last();
+        uint32_t g = 0;
+        bool ok = true;
+        for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
+             u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x)) {
+            const Unit t = decode_unit(sch, u);
+            const int wrow = t.e * N + t.n0;
+            for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
+                const uint32_t slot = g % kStages;
+                const uint32_t ph = (g / kStages) & 1u;
+                if (!__all_sync(0xFFFFFFFFu, wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx,
+                                                          kRoleProducer, slot))) {
+                    ok = false;
+                    break;
                 }
+                const uint32_t fb = bar_full_tma + 8 * slot;
+                ptx::mbar_arrive_expect_tx_elect(fb, Cfg::kMB * kWTileTx + t.n_mma * kBK);
+#pragma unroll
+                for (int mb = 0; mb < Cfg::kMB; ++mb) {
+                    ptx::tma_load_2d_elect(sbase + Cfg::kOffW + (slot * Cfg::kMB + mb) * kWTileBytes,
+                                           &map_w, ks * kBK, wrow + mb * kBW, fb, pol_w);
+                }
+                load_a_rows<false, true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
+                                         ks * kBK, t.row0, t.n_mma, fb, pol_a);
             }
-            // No copy may land after the CTA exits: wait for the last ring's
-            // worth of issued loads (all of them on the normal path already).
-            const uint32_t first = g > kStages ? g - kStages : 0;
-            for (uint32_t gg = first; gg < g; ++gg) {
-                wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
-            }
+        }
+        // No copy may land after the CTA exits: wait for the last ring's
+        // worth of issued loads (all of them on the normal path already).
+        const uint32_t first = g > kStages ? g - kStages : 0;
+        for (uint32_t gg = first; gg < g; ++gg) {
+            wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer ---
-        if (lane == 0) {
-            uint32_t g = 0, tc = 0;
-            bool ok = true;
-            for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
-                 u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x), ++tc) {
-                const Unit t = decode_unit(sch, u);
-                const uint32_t b = tc % Cfg::kAccBufs;
-                if (!wait_bounded(bar_tempty + 8 * b, ((tc / Cfg::kAccBufs) & 1u) ^ 1u, wctx, kRoleMma,
-                                  0x100u | b)) {
+        // The whole warp walks the units and stages with identical values;
+        // every tcgen05 instruction is issued by its elected lane.  Waits
+        // are polled by every lane and agreed on with a vote, so the warp
+        // stays converged and its address and descriptor arithmetic stays
+        // warp-uniform.
+        uint32_t g = 0, tc = 0;
+        bool ok = true;
+        for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
+             u += kCL > 1 ? ngroups : static_cast<int>(gridDim.x), ++tc) {
+            const Unit t = decode_unit(sch, u);
+            const uint32_t b = tc % Cfg::kAccBufs;
+            if (!__all_sync(0xFFFFFFFFu,
+                            wait_bounded(bar_tempty + 8 * b, ((tc / Cfg::kAccBufs) & 1u) ^ 1u, wctx,
+                                         kRoleMma, 0x100u | b))) {
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t idesc0 =
+                ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, kBW, t.n_mma);
+            const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
+            for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
+                const uint32_t slot = g % kStages;
+                const uint32_t ph = (g / kStages) & 1u;
+                const bool ready =
+                    wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) &&
+                    wait_bounded(bar_full_sf + 8 * slot, ph, wctx, kRoleMma, 0x10u | slot);
+                if (!__all_sync(0xFFFFFFFFu, ready)) {
+                    ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t idesc0 =
-                    ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, kBW, t.n_mma);
-                const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
-                for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
-                    const uint32_t slot = g % kStages;
-                    const uint32_t ph = (g / kStages) & 1u;
-                    if (!wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
-                        !wait_bounded(bar_full_sf + 8 * slot, ph, wctx, kRoleMma, 0x10u | slot)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    // scale slot: [weight block 0..MB-1: 4 cols each][token atoms: 4 cols each]
-                    const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
-                    const uint32_t sfb_col = sf_col + 4 * Cfg::kMB;
-                    const uint32_t sfa = sbase + Cfg::kOffSfa + slot * Cfg::kMB * kSfaBytes;
-                    const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
+                // scale slot: [weight block 0..MB-1: 4 cols each][token atoms: 4 cols each]
+                const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
+                const uint32_t sfb_col = sf_col + 4 * Cfg::kMB;
+                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * Cfg::kMB * kSfaBytes;
+                const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
+#pragma unroll
+                for (int mb = 0; mb < Cfg::kMB; ++mb) {
+                    ptx::tc_cp_32x128b_warpx4_elect(sf_col + 4 * mb,
+                                                    ptx::desc_sf_32x16(sfa + mb * kSfaBytes));
+                }
+                ptx::tc_cp_32x128b_warpx4_elect(sfb_col, ptx::desc_sf_32x16(sfb));
+                if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
+                    ptx::tc_cp_32x128b_warpx4_elect(sfb_col + 4, ptx::desc_sf_32x16(sfb + 512));
+                }
+                const uint32_t wsm = sbase + Cfg::kOffW + slot * Cfg::kMB * kWTileBytes;
+                const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 32; ++kk) {
 #pragma unroll
                     for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                        ptx::tc_cp_32x128b_warpx4(sf_col + 4 * mb,
-                                                  ptx::desc_sf_32x16(sfa + mb * kSfaBytes));
+                        ptx::mma_mxf8f6f4_1x_elect(
+                            d_tmem + mb * kTMax,
+                            ptx::desc_kmajor_sw128(wsm + mb * kWTileBytes + kk * 32),
+                            ptx::desc_kmajor_sw128(asm_ + kk * 32),
+                            ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col + 4 * mb, sfb_col,
+                            (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
                     }
-                    ptx::tc_cp_32x128b_warpx4(sfb_col, ptx::desc_sf_32x16(sfb));
-                    if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
-                        ptx::tc_cp_32x128b_warpx4(sfb_col + 4, ptx::desc_sf_32x16(sfb + 512));
-                    }
-                    const uint32_t wsm = sbase + Cfg::kOffW + slot * Cfg::kMB * kWTileBytes;
-                    const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 32; ++kk) {
-#pragma unroll
-                        for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                            ptx::mma_mxf8f6f4_1x(
-                                d_tmem + mb * kTMax,
-                                ptx::desc_kmajor_sw128(wsm + mb * kWTileBytes + kk * 32),
-                                ptx::desc_kmajor_sw128(asm_ + kk * 32),
-                                ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col + 4 * mb, sfb_col,
-                                (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
-                        }
-                    }
-                    ptx::tc_commit(bar_empty + 8 * slot);
                 }
-                if (!ok) break;
-                ptx::tc_commit(bar_tfull + 8 * b);
+                ptx::tc_commit_elect(bar_empty + 8 * slot);
             }
-            // Everything issued must finish before TMEM is released.
-            ptx::tc_commit(bar_done);
-            wait_drain(bar_done, 0u, timeout_ns);
+            if (!ok) break;
+            ptx::tc_commit_elect(bar_tfull + 8 * b);
         }
+        // Everything issued must finish before TMEM is released.
+        ptx::tc_commit_elect(bar_done);
+        wait_drain(bar_done, 0u, timeout_ns);
     } else if (warp >= 4 && warp < 4 + kEpiWarps) {
         // ---------------------------------------------------- epilogue --
         const int q = warp & 3;   // TMEM lane quadrant this warp may read
@@ -1289,7 +1301,7 @@ int gemm_variant_max_experts(int variant) {
 int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms) {
     const long long per = rows / (E > 0 ? E : 1);
     if (per <= 48) {
-        if (num_sms > 0 && rows <= 32LL * E && K >= 512 && N >= kBW) {
+        if (num_sms > 0 && rows <= 32LL * E && K >= kBK && N >= kBW) {
             GemmArgs a{};
             a.E = E;
             a.N = N;

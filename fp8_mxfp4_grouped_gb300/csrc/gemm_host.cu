@@ -68,7 +68,7 @@ hg_status hg_grouped_w4a8_gemm_host(const int32_t* topk_ids_host, const uint8_t*
     if (M < 0 || top_k < 1 || E < 1) return HG_ERR_INVALID_ARG;
     const long long R = static_cast<long long>(M) * top_k;
     if (R > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
-    if (E > hg::gemm_max_experts() || N < 128 || N % 128 != 0 || K < 512 || K % 512 != 0)
+    if (E > hg::gemm_max_experts() || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0)
         return HG_ERR_UNSUPPORTED_SHAPE;
     if (static_cast<long long>(E) * N > 0x7FFFFFFFll) return HG_ERR_UNSUPPORTED_SHAPE;
     if (!w_fp4 || !w_scale || !is_aligned(w_fp4, 32) || !is_aligned(w_scale, 4))

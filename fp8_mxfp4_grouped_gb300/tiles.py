@@ -39,7 +39,7 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     every expert at the mean predicts a 14-15 % gain for the other."""
     per = rows // max(E, 1)
     if per <= 48:
-        if num_sms > 0 and rows <= 32 * E and K >= 512 and N >= W_TILE and split_ctas >= SPLIT_CLUSTER:
+        if num_sms > 0 and rows <= 32 * E and K >= 128 and N >= W_TILE and split_ctas >= SPLIT_CLUSTER:
             units = min(E, rows) * (N // W_TILE)
             KT = K // 128
             if units > 0:
@@ -104,14 +104,16 @@ def units(offsets, N: int, t_max: int = T_MAX):
 
 def choose_split(U: int, KT: int, G: int, max_split: int = SPLIT_CLUSTER) -> int:
     """Mirror of the split-K factor variant 6 takes on the device: with G CTAs
-    and U units of KT stages, the s in {1, 2, 4} that minimises the stages of
-    the busiest CTA, ceil(U / (G / s)) * KT / s; ties keep the smaller s."""
+    and U units of KT stages, the s in {1, 2, 4} dividing KT that minimises the
+    stages of the busiest CTA, ceil(U / (G / s)) * KT / s; ties keep the
+    smaller s."""
     best, best_cost = 1, -(-U // G) * KT
     s = 2
     while s <= max_split:
-        c = -(-U // (G // s)) * (KT // s)
-        if c < best_cost:
-            best, best_cost = s, c
+        if KT % s == 0:
+            c = -(-U // (G // s)) * (KT // s)
+            if c < best_cost:
+                best, best_cost = s, c
         s *= 2
     return best
 

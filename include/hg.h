@@ -5,8 +5,10 @@
  * Every entry point takes plain pointers and sizes.  All array pointers are
  * DEVICE pointers owned by the caller unless stated otherwise; the library
  * never allocates or frees caller memory and never synchronises inside the
- * compute calls, so they can be enqueued on any stream (including inside a
- * CUDA-graph capture).  Errors are returned as hg_status codes; nothing is
+ * compute calls, so they can be enqueued on any stream.  The plan
+ * (hg_plan_expert_offsets), the GEMM (both scale layouts) and the
+ * host-buffer call can also be captured into a CUDA graph and replayed (each
+ * is tested that way).  Errors are returned as hg_status codes; nothing is
  * thrown across this interface.  Argument checks happen before any CUDA call,
  * so a bad argument is reported even on a machine without a GPU.
  *
@@ -39,7 +41,7 @@ typedef struct CUstream_st* hg_stream_t;
 typedef enum {
     HG_OK = 0,
     HG_ERR_INVALID_ARG = 1,       /* null pointer, negative size, misaligned pointer      */
-    HG_ERR_UNSUPPORTED_SHAPE = 2, /* K % 512 != 0, N % 128 != 0, or a size beyond limits  */
+    HG_ERR_UNSUPPORTED_SHAPE = 2, /* K % 128 != 0, N % 128 != 0, or a size beyond limits  */
     HG_ERR_RESOURCE = 3,          /* shared memory does not fit even the smallest block   */
     HG_ERR_CUDA = 4,              /* a CUDA runtime / driver call failed                  */
     HG_ERR_TIMEOUT = 5,           /* device: a bounded wait inside a kernel gave up        */
@@ -56,8 +58,9 @@ int hg_version(void);
 /*
  * Drop the library's per-device state: the cached device properties, the
  * device addresses of its status word and of the no-allocation plan's
- * scratch array, the kernels' shared-memory settings and the
- * cluster-residency answers.  The next call on a device queries them again.
+ * scratch array, the kernels' shared-memory settings, the
+ * cluster-residency answers and the cache of encoded TMA tensor maps (keyed
+ * by base address and shape).  The next call on a device queries them again.
  * Call it before using the library in a new context on a device whose
  * context was destroyed (cudaDeviceReset): the cached addresses and settings
  * belong to the old context.  Frees nothing: the status word and the scratch
@@ -126,12 +129,11 @@ int32_t hg_plan_launches(int32_t M, int32_t top_k, int32_t E);
 
 /*
  * The routing plan without a workspace argument, for callers that cannot
- * call cudaMalloc where they plan: code that runs while a CUDA graph is being
- * captured (an allocation is not a stream operation, so it cannot become part
- * of the graph), hosts that own every device allocation and do not let a
- * library make its own (framework plugins with a planned memory pool), and
- * loops that cannot take cudaMalloc's implicit device synchronisation.  The
- * pages this library follows have no counterpart to this entry point.
+ * call cudaMalloc where they plan: a host framework that owns every device
+ * allocation through its own memory pool and does not let a library allocate
+ * behind its back, or a latency-critical loop that cannot take the
+ * device-wide synchronisation cudaMalloc and cudaFree may imply.  The pages
+ * this library follows have no counterpart to this entry point.
  *
  * Arguments and results are those of hg_plan_expert_offsets without the
  * workspace.  The workspace is instead a fixed 256 KiB array in this
@@ -177,7 +179,7 @@ hg_status hg_plan_expert_offsets_noalloc(const int32_t* topk_ids, int32_t M, int
  *
  * Accumulation is FP32 inside the tensor cores; the scales are applied per
  * 32-K block by the block-scaled MMA.  Supported: E in [1, 512],
- * N % 128 == 0, K % 512 == 0, rows in [0, 2^31).  Offsets that are not
+ * N % 128 == 0, K % 128 == 0, rows in [0, 2^31).  Offsets that are not
  * monotone or exceed rows are detected on the device: the affected experts
  * are skipped and HG_ERR_BAD_OFFSETS is recorded for hg_get_device_status.
  * E2M1/E4M3 NaN codes and E8M0 code 255 are not supported inputs.

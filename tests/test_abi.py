@@ -92,7 +92,9 @@ def test_gemm_argument_validation(lib):
     assert _gemm(lib, off=0) == lib.HG_ERR_INVALID_ARG
     assert _gemm(lib, a=0) == lib.HG_ERR_INVALID_ARG
     assert _gemm(lib, N=200) == lib.HG_ERR_UNSUPPORTED_SHAPE
-    assert _gemm(lib, K=384) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, K=320) == lib.HG_ERR_UNSUPPORTED_SHAPE    # K % 128 != 0
+    assert _gemm(lib, K=64) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert lib.hg_gemm_ctas(4, 256, 320, 32) == 0                # rejected before any device query
     assert _gemm(lib, E=5000) == lib.HG_ERR_UNSUPPORTED_SHAPE
     assert _gemm(lib, E=513) == lib.HG_ERR_UNSUPPORTED_SHAPE   # 512 experts at most
     assert _gemm(lib, w=0x4010) == lib.HG_ERR_INVALID_ARG      # W needs 32-byte alignment
@@ -161,7 +163,7 @@ def test_gemm_host_argument_validation(lib):
     assert call(E=0) == lib.HG_ERR_INVALID_ARG
     assert call(E=513) == lib.HG_ERR_UNSUPPORTED_SHAPE
     assert call(N=200) == lib.HG_ERR_UNSUPPORTED_SHAPE
-    assert call(K=384) == lib.HG_ERR_UNSUPPORTED_SHAPE
+    assert call(K=320) == lib.HG_ERR_UNSUPPORTED_SHAPE
     assert call(M=1 << 30) == lib.HG_ERR_UNSUPPORTED_SHAPE      # M*top_k >= 2^31
     assert call(w=0x4010) == lib.HG_ERR_INVALID_ARG              # W needs 32-byte alignment
     assert call(ws_=0x5001) == lib.HG_ERR_INVALID_ARG

@@ -106,6 +106,10 @@ def test_one_hot_weights_distinct_expert_scales(cuda_lib, variant):
     (3, 256, 2048, [0, 224, 225, 673]),                   # exactly one tile, one row, 3 tiles (448 + 1)
     (4, 128, 512, [0, 0, 0, 33, 33]),                     # leading / trailing empty experts
     (2, 512, 3072, [0, 129, 260]),                        # K = 24 stages: the ring wraps many times
+    (3, 256, 640, [0, 30, 200, 201]),                     # K = 640: 5 stages (no split divides it)
+    (2, 384, 1152, [0, 250, 260]),                        # K = 1152: 9 stages
+    (2, 128, 128, [0, 5, 40]),                            # K = 128: a single stage
+    (1, 256, 384, [0, 77]),                               # K = 384: 3 stages
 ])
 def test_ragged_experts_random_codes(cuda_lib, variant, E, N, K, cuts):
     rng = np.random.default_rng(E * 1000 + K)
@@ -134,9 +138,9 @@ def test_max_experts_mostly_empty(cuda_lib, variant):
 
 @pytest.mark.parametrize("E,cuts", [(1, [0, 1]), (2, [0, 0, 1]), (1, [0, 17])])
 def test_minimum_shapes(cuda_lib, variant, E, cuts):
-    # N = 128 (one weight tile), K = 512 (the smallest supported), one or a few rows
+    # N = 128 (one weight tile), K = 128 (the smallest supported), one or a few rows
     rng = np.random.default_rng(13 + len(cuts) + cuts[-1])
-    N, K = 128, 512
+    N, K = 128, 128
     R = cuts[-1]
     a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
     out = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
@@ -426,7 +430,7 @@ def _random_problem(seed):
     rng = np.random.default_rng(seed)
     E = int(rng.integers(1, 41))
     N = 128 * int(rng.integers(1, 5))
-    K = 512 * int(rng.integers(1, 4))
+    K = 128 * int(rng.integers(1, 13))
     sizes = rng.integers(0, 260, E)
     sizes[rng.random(E) < 0.25] = 0
     cuts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
