@@ -36,9 +36,7 @@ std::atomic<int> g_forced_variant{0};
 int choose_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms) {
     int v = g_forced_variant.load();
     if (!v) v = gemm_pick_variant(E, N, K, rows, num_sms);
-    if (v == 4 && N % 256 != 0) v = 3;   // CTA pairs split 256 weight rows
-    if (v == 5 && N % 256 != 0) v = 2;
-    if (v == 7 && N % 256 != 0) v = 2;   // two 128-row weight blocks per unit
+    if (v == 4 && N % 256 != 0) v = 8;   // CTA pairs split 256 weight rows
     return v;
 }
 
@@ -475,7 +473,9 @@ int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows) {
 }
 
 int32_t hg_set_gemm_variant(int32_t variant) {
-    if (variant < 0 || variant > 8) return -1;
+    if (variant != 0 && variant != 1 && variant != 2 && variant != 4 && variant != 6 &&
+        variant != 8)
+        return -1;
     return g_forced_variant.exchange(variant);
 }
 

@@ -64,19 +64,19 @@ constexpr uint32_t kSmemReservedPerBlock = 1024;
 // K loop of every unit over 2 or CL of them (split-K, chosen on the device
 // from the unit count); each CTA then holds receive slots for the FP32
 // partial tiles of the others.
-// MB: 128-row weight blocks per unit.  With MB = 2 a unit covers 256 weight
-// rows as two M = 128 MMAs per K step that share the stage's token tile (one
-// activation tile per two weight tiles, two accumulators).
 // AB: TMEM accumulator buffers.  With AB = 1 the MMAs of the next unit wait
 // for the epilogue to drain the accumulator (the other CTA on the SM keeps the
 // tensor core busy meanwhile); it lets a 224-row token tile run two CTAs per SM.
-template <int T, int S, int C, int CL = 1, int MB = 1, int AB = 2>
+// SA: the activation boxes of a stage are issued by the stage's scale warp
+// instead of the producer (more warps issuing TMA; measured faster for the
+// 112-row tiles, slower for the 224-row ones).
+template <int T, int S, int C, int CL = 1, int AB = 2, bool SA = false>
 struct GemmCfg {
+    static constexpr bool kScaleWarpsLoadA = SA;
     static constexpr int kTMax = T;
     static constexpr int kStages = S;
     static constexpr int kCtasPerSm = C;
     static constexpr int kCluster = CL;
-    static constexpr int kMB = MB;
     static constexpr int kAccBufs = AB;
     // A CTA of a split group finalises 4/s of the four TMEM lane quadrants
     // and receives s-1 partials of each: (4/s)(s-1) slots, at most 3.
@@ -89,14 +89,14 @@ struct GemmCfg {
     static constexpr uint32_t kATileBytes = T * kBK;
     static constexpr int kSfbAtoms = T > 128 ? 2 : 1;      // 128 tokens per scale block
     static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
-    static constexpr uint32_t kAccCols = MB * T;           // TMEM columns per accumulator buffer
+    static constexpr uint32_t kAccCols = T;               // TMEM columns per accumulator buffer
     static constexpr uint32_t kTmemCols = 512 / C;
     static constexpr uint32_t kSfCol0 = AB * kAccCols;     // scale slots after the buffers
-    static constexpr uint32_t kSfSlotCols = 4 * MB + 4 * kSfbAtoms;
-    static constexpr uint32_t kOffW = 0;                   // [stage][block] weight tiles
-    static constexpr uint32_t kOffA = kOffW + S * MB * kWTileBytes;
+    static constexpr uint32_t kSfSlotCols = 4 + 4 * kSfbAtoms;
+    static constexpr uint32_t kOffW = 0;                   // [stage] weight tiles
+    static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
     static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
-    static constexpr uint32_t kOffSfb = kOffSfa + S * MB * kSfaBytes;
+    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;
     static constexpr uint32_t kOffRx = kOffSfb + S * kSfbBytes;
     static constexpr uint32_t kOffBar = kOffRx + kRxBytes;
     static constexpr uint32_t kOffMisc = kOffBar + 256;
@@ -107,7 +107,6 @@ struct GemmCfg {
     static constexpr size_t kSmemBudget =
         C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
     static_assert(CL == 1 || CL == 2 || CL == 4, "split over 2 or 4 CTAs");
-    static_assert(MB == 1 || (MB == 2 && CL == 1), "two weight blocks per unit, without split-K");
     static_assert(AB == 2 || (AB == 1 && CL == 1), "one accumulator buffer, without split-K");
     static_assert(8 * (3 * S + 5 + 8) <= 256, "barrier area");
     // experts whose scheduler tables still fit next to the ring (<= kMaxE)
@@ -163,14 +162,11 @@ struct PairCfg {
 };
 
 using CfgPair = PairCfg<224, 5, 1>;     // many rows per expert, N % 256 == 0
-using CfgPairMid = PairCfg<96, 4, 2>;   // CTA pairs, two pipelines per SM
 
 using CfgSmall = GemmCfg<64, 4, 2>;    // few rows per expert: HBM-bound weight streaming
-using CfgMid = GemmCfg<112, 3, 2>;     // a few hundred rows per expert
-using CfgLarge = GemmCfg<224, 4, 1>;   // many rows per expert: tensor-bound
+using CfgMid = GemmCfg<112, 3, 2, 1, 2, true>;   // a few hundred rows per expert
 using CfgSplit = GemmCfg<32, 4, 2, 4>; // few units per CTA: split-K over clusters of 4
-using CfgDual = GemmCfg<112, 4, 1, 1, 2>;   // 256 weight rows per unit, one token tile shared
-using CfgWide2 = GemmCfg<224, 2, 2, 1, 1, 1>;   // 224-row tiles, two CTAs per SM, one TMEM buffer each
+using CfgWide2 = GemmCfg<224, 2, 2, 1, 1>;   // 224-row tiles, two CTAs per SM, one TMEM buffer each
 
 // Split-K factor for a launch of G CTAs (a multiple of max_split) over U
 // units of KT stages: the s in {1, 2, 4} dividing KT that minimises the
@@ -264,7 +260,9 @@ __device__ __forceinline__ void load_a_rows(const AMaps& maps, uint32_t dst, int
     for (int i = 3; i >= 0; --i) {
         const int h = 16 << i;
         if (n & h) {
-            if (kPair) {
+            if (kPair && kElect) {
+                ptx::tma_load_2d_pair_elect(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
+            } else if (kPair) {
                 ptx::tma_load_2d_pair(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
             } else if (kElect) {
                 ptx::tma_load_2d_elect(dst + r * kBK, &maps.box[i], k, row + r, bar, policy);
@@ -342,7 +340,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     }
 
     // Per-expert token tiling, from the expert's own row count.
-    const int NT = N / (kBW * Cfg::kMB);
+    const int NT = N / kBW;
     for (int e = threadIdx.x; e < E; e += Cfg::kThreads) {
         const int lo = offsets[e];
         const int hi = offsets[e + 1];
@@ -387,7 +385,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     ptx::tc_fence_after();
 
     const uint32_t tmem_base = misc[0];
-    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT, kBW * Cfg::kMB};
+    const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT, kBW};
     const int U = s_prefix[E];
     const int KT = K / kBK;
     const WaitCtx wctx{status, misc + 1, timeout_ns};
@@ -428,14 +426,13 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     break;
                 }
                 const uint32_t fb = bar_full_tma + 8 * slot;
-                ptx::mbar_arrive_expect_tx_elect(fb, Cfg::kMB * kWTileTx + t.n_mma * kBK);
-#pragma unroll
-                for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                    ptx::tma_load_2d_elect(sbase + Cfg::kOffW + (slot * Cfg::kMB + mb) * kWTileBytes,
-                                           &map_w, ks * kBK, wrow + mb * kBW, fb, pol_w);
+                ptx::mbar_arrive_expect_tx_elect(fb, kWTileTx + t.n_mma * kBK);
+                ptx::tma_load_2d_elect(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w, ks * kBK,
+                                       wrow, fb, pol_w);
+                if constexpr (!Cfg::kScaleWarpsLoadA) {
+                    load_a_rows<false, true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
+                                             ks * kBK, t.row0, t.n_mma, fb, pol_a);
                 }
-                load_a_rows<false, true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
-                                         ks * kBK, t.row0, t.n_mma, fb, pol_a);
             }
         }
         // No copy may land after the CTA exits: wait for the last ring's
@@ -477,33 +474,25 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                     break;
                 }
                 ptx::tc_fence_after();
-                // scale slot: [weight block 0..MB-1: 4 cols each][token atoms: 4 cols each]
+                // scale slot: [weight block: 4 cols][token atoms: 4 cols each]
                 const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
-                const uint32_t sfb_col = sf_col + 4 * Cfg::kMB;
-                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * Cfg::kMB * kSfaBytes;
+                const uint32_t sfb_col = sf_col + 4;
+                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
                 const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
-#pragma unroll
-                for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                    ptx::tc_cp_32x128b_warpx4_elect(sf_col + 4 * mb,
-                                                    ptx::desc_sf_32x16(sfa + mb * kSfaBytes));
-                }
+                ptx::tc_cp_32x128b_warpx4_elect(sf_col, ptx::desc_sf_32x16(sfa));
                 ptx::tc_cp_32x128b_warpx4_elect(sfb_col, ptx::desc_sf_32x16(sfb));
                 if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
                     ptx::tc_cp_32x128b_warpx4_elect(sfb_col + 4, ptx::desc_sf_32x16(sfb + 512));
                 }
-                const uint32_t wsm = sbase + Cfg::kOffW + slot * Cfg::kMB * kWTileBytes;
+                const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
                 const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 32; ++kk) {
-#pragma unroll
-                    for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                        ptx::mma_mxf8f6f4_1x_elect(
-                            d_tmem + mb * kTMax,
-                            ptx::desc_kmajor_sw128(wsm + mb * kWTileBytes + kk * 32),
-                            ptx::desc_kmajor_sw128(asm_ + kk * 32),
-                            ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col + 4 * mb, sfb_col,
-                            (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
-                    }
+                    ptx::mma_mxf8f6f4_1x_elect(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
+                                               ptx::desc_kmajor_sw128(asm_ + kk * 32),
+                                               ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
+                                               sfb_col,
+                                               (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
                 }
                 ptx::tc_commit_elect(bar_empty + 8 * slot);
             }
@@ -538,20 +527,17 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
             if constexpr (kCL == 1) {
+                const int n = t.n0 + 32 * q + lane;
+                uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
+                for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+                    uint32_t v[16];
+                    ptx::tmem_ld_32x32b_x16(taddr + c0, v);
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                    const int n = t.n0 + mb * kBW + 32 * q + lane;
-                    uint16_t* dst = out + static_cast<size_t>(t.row0) * N + n;
-                    for (int c0 = 0; c0 < t.nrows; c0 += 16) {
-                        uint32_t v[16];
-                        ptx::tmem_ld_32x32b_x16(taddr + mb * kTMax + c0, v);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (c0 + j < t.nrows) {
-                                dst[static_cast<size_t>(c0 + j) * N] = __bfloat16_as_ushort(
-                                    __float2bfloat16_rn(__uint_as_float(v[j])));
-                            }
+                    for (int j = 0; j < 16; ++j) {
+                        if (c0 + j < t.nrows) {
+                            dst[static_cast<size_t>(c0 + j) * N] = __bfloat16_as_ushort(
+                                __float2bfloat16_rn(__uint_as_float(v[j])));
                         }
                     }
                 }
@@ -650,6 +636,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         // ------------------------------------------- scale staging -----
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;   // warps 2, 3, 8, 9, ...
         const int ws_row = K / 32;     // bytes per w_scale row
+        const uint64_t pol_a = ptx::policy_evict_last();
         uint32_t g = 0;
         bool ok = true;
         for (int u = kCL > 1 ? gid : static_cast<int>(blockIdx.x); ok && u < U;
@@ -662,14 +649,10 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 const uint32_t ph = (g / kStages) & 1u;
                 // Weight scales: row n = lane + 32c, the four 32-K blocks of
                 // this stage in one 32-bit word (byte i = block i).
-                uint32_t wv[Cfg::kMB][4];
+                uint32_t wv[4];
 #pragma unroll
-                for (int mb = 0; mb < Cfg::kMB; ++mb) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        wv[mb][c] = ldg_u32(wsrc + static_cast<size_t>(mb * kBW + 32 * c) * ws_row +
-                                            ks * 4);
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    wv[c] = ldg_u32(wsrc + static_cast<size_t>(32 * c) * ws_row + ks * 4);
                 }
                 // Token scales: one per 128-K group, replicated into the four
                 // 32-K blocks.  Token index = 128a + lane + 32c.
@@ -686,17 +669,20 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                                 0x01010101u;
                     }
                 }
-                if (!wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleScale, slot)) {
+                if (!__all_sync(0xFFFFFFFFu,
+                                wait_bounded(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleScale, slot))) {
                     ok = false;
                     break;
                 }
-                const uint32_t sfa =
-                    sbase + Cfg::kOffSfa + slot * Cfg::kMB * kSfaBytes + 16 * lane;
-                const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes + 16 * lane;
-#pragma unroll
-                for (int mb = 0; mb < Cfg::kMB; ++mb) {
-                    sts_v4(sfa + mb * kSfaBytes, wv[mb][0], wv[mb][1], wv[mb][2], wv[mb][3]);
+                if constexpr (Cfg::kScaleWarpsLoadA) {
+                    // counted on the stage's full barrier, armed by the producer
+                    load_a_rows<false, true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
+                                             ks * kBK, t.row0, t.n_mma, bar_full_tma + 8 * slot,
+                                             pol_a);
                 }
+                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes + 16 * lane;
+                const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes + 16 * lane;
+                sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
                 sts_v4(sfb, av[0], av[1], av[2], av[3]);
                 if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
                     sts_v4(sfb + 512, av[4 % (4 * Cfg::kSfbAtoms)], av[5 % (4 * Cfg::kSfbAtoms)],
@@ -705,6 +691,14 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar_full_sf + 8 * slot);
+            }
+        }
+        if (Cfg::kScaleWarpsLoadA && !ok) {
+            // Gave up (a wait timed out): activation boxes this warp issued
+            // may belong to stages nobody consumes, so nothing waits for
+            // them; give them time to land before the CTA can exit.
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (ptx::globaltimer_ns() - t0 < 50000u) {
             }
         }
     }
@@ -861,51 +855,51 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
-        if (lane == 0) {
-            const uint64_t pol_w = ptx::policy_evict_last();   // weight tiles are re-read by the other token tiles of their expert
-            const uint64_t pol_a = ptx::policy_evict_last();
-            const uint32_t full_tma_leader = ptx::mapa_shared(bar_full_tma, 0);
-            uint32_t g = 0;
-            bool ok = true;
-            for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
-                 u += static_cast<int>(gridDim.x >> 1)) {
-                int e, wrow0, row0, nrows, n_mma;
-                unit_of(u, e, wrow0, row0, nrows, n_mma);
-                const int half = n_mma / 2;
-                const int wrow = e * N + wrow0 + static_cast<int>(rank) * kBW;
-                const int arow = row0 + static_cast<int>(rank) * half;
-                for (int ks = 0; ks < KT; ++ks, ++g) {
-                    const uint32_t slot = g % kStages;
-                    const uint32_t ph = (g / kStages) & 1u;
-                    if (!wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleProducer, slot)) {
-                        ok = false;
-                        break;
-                    }
-                    // both CTAs' bytes land on the leader's barrier
-                    const uint32_t fb = full_tma_leader + 8 * slot;
-                    if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * (kWTileTx + half * kBK));
-                    ptx::tma_load_2d_pair(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w,
-                                          ks * kBK, wrow, fb, pol_w);
-                    load_a_rows<true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
-                                      ks * kBK, arow, half, fb, pol_a);
+        // Whole converged warp; the elected lane issues (see the plain
+        // kernel's producer).
+        const uint64_t pol_w = ptx::policy_evict_last();   // weight tiles are re-read by the other token tiles of their expert
+        const uint32_t full_tma_leader = ptx::mapa_shared(bar_full_tma, 0);
+        uint32_t g = 0;
+        bool ok = true;
+        for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
+             u += static_cast<int>(gridDim.x >> 1)) {
+            int e, wrow0, row0, nrows, n_mma;
+            unit_of(u, e, wrow0, row0, nrows, n_mma);
+            const int half = n_mma / 2;
+            const int wrow = e * N + wrow0 + static_cast<int>(rank) * kBW;
+            for (int ks = 0; ks < KT; ++ks, ++g) {
+                const uint32_t slot = g % kStages;
+                const uint32_t ph = (g / kStages) & 1u;
+                if (!__all_sync(0xFFFFFFFFu, wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx,
+                                                                kRoleProducer, slot))) {
+                    ok = false;
+                    break;
                 }
+                // both CTAs' bytes land on the leader's barrier; the stage's
+                // scale warp issues the activation boxes (more warps issuing
+                // TMA per SM: measured 1-3 % faster at large M)
+                const uint32_t fb = full_tma_leader + 8 * slot;
+                if (leader) ptx::mbar_arrive_expect_tx_elect(fb, 2 * (kWTileTx + half * kBK));
+                ptx::tma_load_2d_pair_elect(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w,
+                                            ks * kBK, wrow, fb, pol_w);
             }
-            // No copy may land after the CTA exits.  The leader sees its
-            // stages complete on bar_full_tma; the odd CTA only through the
-            // leader's release of the slot (bar_empty), once it consumed it.
-            const uint32_t first = g > kStages ? g - kStages : 0;
-            for (uint32_t gg = first; gg < g; ++gg) {
-                if (leader) {
-                    wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
-                } else {
-                    // the leader's commit of stage gg completes phase gg / S
-                    wait_drain(bar_empty + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
-                }
+        }
+        // No copy may land after the CTA exits.  The leader sees its
+        // stages complete on bar_full_tma; the odd CTA only through the
+        // leader's release of the slot (bar_empty), once it consumed it.
+        const uint32_t first = g > kStages ? g - kStages : 0;
+        for (uint32_t gg = first; gg < g; ++gg) {
+            if (leader) {
+                wait_drain(bar_full_tma + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
+            } else {
+                // the leader's commit of stage gg completes phase gg / S
+                wait_drain(bar_empty + 8 * (gg % kStages), (gg / kStages) & 1u, timeout_ns);
             }
         }
     } else if (warp == 1) {
-        if (leader && lane == 0) {
+        if (leader) {
             // --------------------------------------- MMA issuer (pair) ---
+            // Whole converged warp of the even CTA; the elected lane issues.
             uint32_t g = 0, tc = 0;
             bool ok = true;
             for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
@@ -913,8 +907,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 int e, wrow0, row0, nrows, n_mma;
                 unit_of(u, e, wrow0, row0, nrows, n_mma);
                 const uint32_t b = tc & 1u;
-                if (!wait_bounded<true>(bar_tempty + 8 * b, ((tc >> 1) & 1u) ^ 1u, wctx, kRoleMma,
-                                        0x100u | b)) {
+                if (!__all_sync(0xFFFFFFFFu,
+                                wait_bounded<true>(bar_tempty + 8 * b, ((tc >> 1) & 1u) ^ 1u, wctx,
+                                                   kRoleMma, 0x100u | b))) {
                     break;
                 }
                 ptx::tc_fence_after();
@@ -924,9 +919,11 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 for (int ks = 0; ks < KT; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
-                    if (!wait_bounded<true>(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) ||
-                        !wait_bounded<true>(bar_full_sf + 8 * slot, ph, wctx, kRoleMma,
-                                            0x10u | slot)) {
+                    const bool ready =
+                        wait_bounded<true>(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) &&
+                        wait_bounded<true>(bar_full_sf + 8 * slot, ph, wctx, kRoleMma,
+                                           0x10u | slot);
+                    if (!__all_sync(0xFFFFFFFFu, ready)) {
                         ok = false;
                         break;
                     }
@@ -934,27 +931,29 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                     const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
                     const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
                     const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
-                    ptx::tc_cp_32x128b_warpx4_pair(sf_col, ptx::desc_sf_32x16(sfa));
-                    ptx::tc_cp_32x128b_warpx4_pair(sf_col + 4, ptx::desc_sf_32x16(sfb));
+                    ptx::tc_cp_32x128b_warpx4_pair_elect(sf_col, ptx::desc_sf_32x16(sfa));
+                    ptx::tc_cp_32x128b_warpx4_pair_elect(sf_col + 4, ptx::desc_sf_32x16(sfb));
                     if (Cfg::kSfbAtoms > 1 && n_mma > 128) {
-                        ptx::tc_cp_32x128b_warpx4_pair(sf_col + 8, ptx::desc_sf_32x16(sfb + 512));
+                        ptx::tc_cp_32x128b_warpx4_pair_elect(sf_col + 8,
+                                                             ptx::desc_sf_32x16(sfb + 512));
                     }
                     const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
                     const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk) {
-                        ptx::mma_mxf8f6f4_1x_pair(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
-                                                  ptx::desc_kmajor_sw128(asm_ + kk * 32),
-                                                  ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
-                                                  sf_col + 4, (ks | kk) != 0 ? 1u : 0u);
+                        ptx::mma_mxf8f6f4_1x_pair_elect(
+                            d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
+                            ptx::desc_kmajor_sw128(asm_ + kk * 32),
+                            ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col, sf_col + 4,
+                            (ks | kk) != 0 ? 1u : 0u);
                     }
-                    ptx::tc_commit_pair_multicast(bar_empty + 8 * slot, 0x3);
+                    ptx::tc_commit_pair_multicast_elect(bar_empty + 8 * slot, 0x3);
                 }
                 if (!ok) break;
-                ptx::tc_commit_pair_multicast(bar_tfull + 8 * b, 0x3);
+                ptx::tc_commit_pair_multicast_elect(bar_tfull + 8 * b, 0x3);
             }
             // Everything issued must finish before either CTA releases TMEM.
-            ptx::tc_commit_pair_multicast(bar_done, 0x1);
+            ptx::tc_commit_pair_multicast_elect(bar_done, 0x1);
             wait_drain(bar_done, 0u, timeout_ns);
         }
     } else if (warp >= 4 && warp < 4 + kEpiWarps) {
@@ -996,6 +995,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;
         const int ws_row = K / 32;
         const uint32_t full_sf_leader = ptx::mapa_shared(bar_full_sf, 0);
+        const uint32_t full_tma_leader = ptx::mapa_shared(bar_full_tma, 0);
+        const uint64_t pol_a = ptx::policy_evict_last();
         uint32_t g = 0;
         bool ok = true;
         for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
@@ -1027,10 +1028,16 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                                 0x01010101u;
                     }
                 }
-                if (!wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx, kRoleScale, slot)) {
+                if (!__all_sync(0xFFFFFFFFu, wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx,
+                                                                kRoleScale, slot))) {
                     ok = false;
                     break;
                 }
+                // this CTA's half of the token tile, counted on the leader's
+                // full barrier (armed by the leader's producer for both CTAs)
+                load_a_rows<true, true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
+                                        ks * kBK, row0 + static_cast<int>(rank) * (n_mma / 2),
+                                        n_mma / 2, full_tma_leader + 8 * slot, pol_a);
                 const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes + 16 * lane;
                 const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes + 16 * lane;
                 sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
@@ -1048,6 +1055,14 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                         ptx::mbar_arrive_remote(full_sf_leader + 8 * slot);
                     }
                 }
+            }
+        }
+        if (!ok) {
+            // Gave up (a wait timed out): activation boxes this warp issued
+            // may belong to stages nobody consumes, so nothing waits for
+            // them; give them time to land before the CTA can exit.
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (ptx::globaltimer_ns() - t0 < 50000u) {
             }
         }
     }
@@ -1180,7 +1195,7 @@ cudaError_t set_smem_attr(Kern* fn, size_t bytes) {
 template <class Cfg>
 long long grid_plain(const GemmArgs& a) {
     long long grid = static_cast<long long>(a.num_sms) * Cfg::kCtasPerSm;
-    const long long u = units_upper(a, Cfg::kTMax, kBW * Cfg::kMB);
+    const long long u = units_upper(a, Cfg::kTMax, kBW);
     return u < grid ? u : grid;
 }
 
@@ -1280,9 +1295,7 @@ int gemm_variant_max_experts(int variant) {
     switch (variant) {
         case 1: return CfgSmall::kMaxExperts;
         case 2: return CfgMid::kMaxExperts;
-        case 3: return CfgLarge::kMaxExperts;
         case 6: return CfgSplit::kMaxExperts;
-        case 7: return CfgDual::kMaxExperts;
         case 8: return CfgWide2::kMaxExperts;
         default: return kMaxE;
     }
@@ -1290,10 +1303,11 @@ int gemm_variant_max_experts(int variant) {
 
 // Variant choice from the mean rows per expert (the per-expert counts live on
 // the device).  Few rows: weight streaming dominates and two small pipelines
-// per SM keep the MMA issue rate up; many rows: the widest token tile, two
-// CTAs per SM with one TMEM accumulator each (measured faster than one CTA
-// per SM with two accumulators above ~200 rows per expert), with a wave
-// model moving the boundary when the device is known.  With
+// per SM keep the MMA issue rate up; many rows: the widest token tile on CTA
+// pairs (256 weight rows x 224 tokens per MMA; measured faster than every
+// other shape from ~256 rows per expert up, at every configured size), or,
+// when N is not a multiple of 256, 224-row tiles with two CTAs per SM; a
+// wave model moves the boundary when the device is known.  With
 // at most 32 rows per expert the split-K variant is taken when, counting one
 // token tile per active expert (at most min(E, rows) of them), it leaves the
 // busiest CTA at least 15 % fewer stages than variant 1 (num_sms = 0: no
@@ -1323,16 +1337,20 @@ int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms
         }
         return 1;
     }
-    // Above 48 rows per expert: variant 2 (112-row tiles, two accumulators)
-    // or variant 8 (224-row tiles, one accumulator), both two CTAs per SM.
-    // Wave model with every expert at the mean: rounds = units / resident
-    // CTAs rounded up; a variant-8 round costs 1.25 + 0.0026 * tile rows
-    // variant-2 rounds (measured at 112-224 rows per expert).  Skewed
-    // routing leaves more partial tiles than the model counts, so the model
-    // only moves the 192-row default when it predicts a 14 % gain (to the
-    // larger tile) or a 15 % one (to the smaller).
-    const int def = per <= 192 ? 2 : 8;
-    if (num_sms <= 0 || N < kBW) return def;
+    // Above 48 rows per expert: variant 2 (112-row tiles, two CTAs per SM)
+    // or the large-tile variant (4: CTA pairs; 8 when N % 256 != 0).  A
+    // sweep of every configured shape found the large tile faster from 288
+    // rows per expert up and variant 2 faster at 128-256 rows, except where
+    // balanced experts fill the large tiles evenly (12 experts at 170 rows:
+    // 7.5 % faster).  At most 256 rows per expert a wave model decides:
+    // with every expert at the mean, rounds = units / resident CTAs rounded
+    // up, counted in 224-row tiles of 128 weight rows over two CTAs per SM;
+    // a large-tile round costs 1.25 + 0.0026 * tile rows variant-2 rounds,
+    // and the large tile is taken only for a predicted gain of 14 % or more
+    // (skewed routing leaves more partial tiles than the model counts).
+    const int large = N % (2 * kBW) == 0 ? 4 : 8;
+    if (per > 256) return large;
+    if (num_sms <= 0 || N < kBW) return 2;
     const long long g = 2LL * num_sms;
     const long long blocks = static_cast<long long>(E) * (N / kBW);
     const long long t2 = (per + CfgMid::kTMax - 1) / CfgMid::kTMax;
@@ -1340,19 +1358,15 @@ int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms
     const long long rows8 = ((per + t8 - 1) / t8 + 15) / 16 * 16;
     const long long c2 = (blocks * t2 + g - 1) / g * 10000;
     const long long c8 = (blocks * t8 + g - 1) / g * (12500 + 26 * rows8);
-    if (def == 2) return 100 * c8 <= 86 * c2 ? 8 : 2;
-    return 100 * c8 >= 118 * c2 ? 2 : 8;
+    return 100 * c8 <= 86 * c2 ? large : 2;
 }
 
 int gemm_variant_token_tile(int variant) {
     switch (variant) {
         case 1: return CfgSmall::kTMax;
         case 2: return CfgMid::kTMax;
-        case 3: return CfgLarge::kTMax;
         case 4: return CfgPair::kTMax;
-        case 5: return CfgPairMid::kTMax;
         case 6: return CfgSplit::kTMax;
-        case 7: return CfgDual::kTMax;
         case 8: return CfgWide2::kTMax;
         default: return 0;
     }
@@ -1363,11 +1377,8 @@ size_t gemm_smem_bytes(int variant, int32_t E) {
         case 1: return CfgSmall::smem_bytes(E);
         case 2: return CfgMid::smem_bytes(E);
         case 4: return CfgPair::smem_bytes(E);
-        case 5: return CfgPairMid::smem_bytes(E);
         case 6: return CfgSplit::smem_bytes(E);
-        case 7: return CfgDual::smem_bytes(E);
-        case 8: return CfgWide2::smem_bytes(E);
-        default: return CfgLarge::smem_bytes(E);
+        default: return CfgWide2::smem_bytes(E);
     }
 }
 
@@ -1376,11 +1387,8 @@ long long gemm_launch_ctas(const GemmArgs& a) {
         case 1: return grid_plain<CfgSmall>(a);
         case 2: return grid_plain<CfgMid>(a);
         case 4: return grid_pair<CfgPair>(a);
-        case 5: return grid_pair<CfgPairMid>(a);
         case 6: return grid_cluster<CfgSplit>(a);
-        case 7: return grid_plain<CfgDual>(a);
-        case 8: return grid_plain<CfgWide2>(a);
-        default: return grid_plain<CfgLarge>(a);
+        default: return grid_plain<CfgWide2>(a);
     }
 }
 
@@ -1390,11 +1398,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, con
         case 1: return launch_cfg<CfgSmall>(a, map_w, map_a, stream);
         case 2: return launch_cfg<CfgMid>(a, map_w, map_a, stream);
         case 4: return launch_pair<CfgPair>(a, map_w, map_a, stream);
-        case 5: return launch_pair<CfgPairMid>(a, map_w, map_a, stream);
         case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, stream);
-        case 7: return launch_cfg<CfgDual>(a, map_w, map_a, stream);
-        case 8: return launch_cfg<CfgWide2>(a, map_w, map_a, stream);
-        default: return launch_cfg<CfgLarge>(a, map_w, map_a, stream);
+        default: return launch_cfg<CfgWide2>(a, map_w, map_a, stream);
     }
 }
 

@@ -362,6 +362,63 @@ __device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const CUtensorMa
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_pair_elect(uint32_t dst, const CUtensorMap* map,
+                                                       int32_t x, int32_t y, uint32_t cluster_bar,
+                                                       uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8f6f4_1x_pair_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                           uint64_t b_desc, uint32_t idesc,
+                                                           uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair_elect(uint32_t taddr, uint64_t s_desc) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(s_desc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_multicast_elect(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;\n\t}" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_2d_elect(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n\t}" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2_elect(const void* p, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.prefetch.L2.global [%0], %1;\n\t}" ::"l"(reinterpret_cast<uint64_t>(p)),
+        "r"(bytes)
+        : "memory");
+}
+
 // --------------------------------------------------------- descriptors ---
 
 // Shared-memory matrix descriptor: start address, leading / stride byte

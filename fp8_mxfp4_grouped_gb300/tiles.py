@@ -20,8 +20,8 @@ T_MAX depends on the pipeline variant the library picks from rows / E
 from __future__ import annotations
 
 T_MAX = 224
-VARIANT_T_MAX = {1: 64, 2: 112, 3: 224, 4: 224, 5: 96, 6: 32, 7: 112, 8: 224}
-VARIANT_STEP = {1: 16, 2: 16, 3: 16, 4: 32, 5: 32, 6: 16, 7: 16, 8: 16}   # CTA pairs split the token tile in two
+VARIANT_T_MAX = {1: 64, 2: 112, 4: 224, 6: 32, 8: 224}
+VARIANT_STEP = {1: 16, 2: 16, 4: 32, 6: 16, 8: 16}   # CTA pairs split the token tile in two
 SPLIT_CLUSTER = 4        # variant 6: clusters of 4 CTAs, two per SM
 MMA_N_STEP = 16
 W_TILE = 128
@@ -34,9 +34,10 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     With a device (num_sms > 0, split_ctas = the split-K variant's resident
     CTAs) and at most 32 rows per expert, variant 6 is taken when, counting
     one token tile per active expert, it leaves the busiest CTA at least 15 %
-    fewer stages than variant 1.  Above 48 rows per expert the default
-    (variant 2 up to 192 rows, variant 8 above) moves when a wave model with
-    every expert at the mean predicts a 14-15 % gain for the other."""
+    fewer stages than variant 1.  Above 256 rows per expert the large-tile
+    variant (4 on CTA pairs, or 8 when N % 256 != 0); from 49 to 256 rows
+    variant 2, unless a wave model with every expert at the mean predicts a
+    gain of 14 % or more for the large tile."""
     per = rows // max(E, 1)
     if per <= 48:
         if num_sms > 0 and rows <= 32 * E and K >= 128 and N >= W_TILE and split_ctas >= SPLIT_CLUSTER:
@@ -50,12 +51,15 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
                 if 20 * c6 <= 17 * c1:
                     return 6
         return 1
-    default = 2 if per <= 192 else 8
+    large = 4 if N % (2 * W_TILE) == 0 else 8
+    if per > 256:
+        return large
     if num_sms <= 0 or N < W_TILE:
-        return default
-    # wave model with every expert at the mean; a variant-8 round costs
-    # 1.25 + 0.0026 * tile rows variant-2 rounds; moves the default only
-    # for a predicted 14 % gain (to variant 8) or 15 % (to variant 2)
+        return 2
+    # wave model with every expert at the mean, in 224-row tiles of 128
+    # weight rows over two CTAs per SM; a large-tile round costs
+    # 1.25 + 0.0026 * tile rows variant-2 rounds; the large tile only for a
+    # predicted gain of 14 % or more
     g = 2 * num_sms
     blocks = E * (N // W_TILE)
     t2 = -(-per // VARIANT_T_MAX[2])
@@ -63,9 +67,7 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     rows8 = -(-(-(-per // t8)) // 16) * 16
     c2 = -(-(blocks * t2) // g) * 10000
     c8 = -(-(blocks * t8) // g) * (12500 + 26 * rows8)
-    if default == 2:
-        return 8 if 100 * c8 <= 86 * c2 else 2
-    return 2 if 100 * c8 >= 118 * c2 else 8
+    return large if 100 * c8 <= 86 * c2 else 2
 
 
 def expert_tiling(rows_e: int, t_max: int = T_MAX, step: int = MMA_N_STEP):

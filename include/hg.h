@@ -211,10 +211,10 @@ hg_status hg_grouped_w4a8_gemm_mmajor(const uint8_t* a_fp8, const uint8_t* a_sca
 /*
  * Largest token tile (MMA N) hg_grouped_w4a8_gemm uses for these arguments:
  * an expert with r rows is cut into ceil(r / T) tiles of equal size rounded
- * up to 16 rows.  The choice can depend on the current device's SM count
- * and cluster occupancy, which this asks for when a device is present
- * (without one, the split-K variant is never chosen and the boundary between
- * the 112- and 224-row tiles stays at 192 rows per expert).  Launches
+ * up to 16 rows (32 on CTA pairs).  The choice can depend on the current
+ * device's SM count and cluster occupancy, which this asks for when a
+ * device is present (without one, the split-K variant is never chosen and
+ * the 224-row tiles are used exactly above 256 rows per expert).  Launches
  * nothing; 0 for invalid arguments.
  */
 int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows);
@@ -231,19 +231,17 @@ int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows);
 /*
  * Force the GEMM pipeline variant for later calls in this process: 0 = choose
  * automatically (default), 1 = 64-row token tiles with two CTAs per SM,
- * 2 = 112-row tiles with two CTAs per SM, 3 = 224-row tiles with one CTA per
- * SM, 4 = 224-row tiles on CTA pairs (256 weight rows per pair; used only
- * when N % 256 == 0, else variant 3), 5 = 96-row tiles on CTA pairs with two
- * pairs per SM pair (N % 256 == 0, else variant 2), 6 = 32-row tiles with two
- * CTAs per SM in clusters of four that split the K loop of each tile over 1,
- * 2 or 4 CTAs (chosen on the device to even out the work when there are few
- * tiles per CTA; the partial sums are added in a fixed order, so results do
- * not vary from run to run), 7 = 112-row tiles with one CTA per SM and 256
- * weight rows per tile (two 128-row MMAs sharing each token tile; N % 256 ==
- * 0, else variant 2), 8 = 224-row tiles with two CTAs per SM and one TMEM
- * accumulator each.  Meant for tests and tuning.  Returns the
- * previous setting, or -1 for an invalid value (setting unchanged).
- * Host-only.
+ * 2 = 112-row tiles with two CTAs per SM, 4 = 224-row tiles on CTA pairs
+ * (tcgen05 cta_group::2: 256 weight rows per MMA; used only when
+ * N % 256 == 0, else variant 8), 6 = 32-row tiles with two CTAs per SM in
+ * clusters of four that split the K loop of each tile over 1, 2 or 4 CTAs
+ * (chosen on the device to even out the work when there are few tiles per
+ * CTA; the partial sums are added in a fixed order, so results do not vary
+ * from run to run), 8 = 224-row tiles with two CTAs per SM and one TMEM
+ * accumulator each.  (The numbers 3, 5 and 7 belonged to shapes that were
+ * never the fastest and are rejected.)  Meant for tests and tuning.
+ * Returns the previous setting, or -1 for an invalid value (setting
+ * unchanged).  Host-only.
  */
 int32_t hg_set_gemm_variant(int32_t variant);
 

@@ -17,7 +17,7 @@ from tests.gpu_util import assert_rows_close, bf16_bits, np_u8
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [1, 2, 3, 4, 5, 6, 7, 8]   # see hg_set_gemm_variant
+VARIANTS = [1, 2, 4, 6, 8]   # see hg_set_gemm_variant
 
 
 @pytest.fixture(params=VARIANTS, ids=lambda v: f"variant{v}")
@@ -286,8 +286,10 @@ def _sample_rows(off, rng, t_max, per_expert=3, max_experts=6):
     for e in sorted(pick):
         lo, hi = int(off[e]), int(off[e + 1])
         rows |= {lo, hi - 1}
-        for r0, valid, _ in token_tiles(hi - lo, t_max):
-            rows |= {lo + r0, lo + r0 + valid - 1}
+        # tiles are rounded to 16 rows, or 32 on CTA pairs (224-row tiles)
+        for step in ((16, 32) if t_max == 224 else (16,)):
+            for r0, valid, _ in token_tiles(hi - lo, t_max, step):
+                rows |= {lo + r0, lo + r0 + valid - 1}
         rows |= set(int(x) for x in rng.integers(lo, hi, per_expert))
     return np.array(sorted(rows), dtype=np.int64)
 
@@ -313,7 +315,6 @@ def test_full_size_sampled_rows(cuda_lib, cid, M, proj, routing):
     assert np.array_equal(off_t.cpu().numpy(), off)
     rng = np.random.default_rng(cid * 100000 + M)
     rows = _sample_rows(off, rng, cuda_lib.hg_gemm_token_tile(c.E, c.N, c.K, c.R))
-    # (token-tile boundaries are sampled with 16-row rounding; pairs round to 32 rows)
     rr = torch.from_numpy(rows).cuda()
     a = c.a_fp8[rr].cpu().numpy()
     a_s = c.a_scale[rr].cpu().numpy()

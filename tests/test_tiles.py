@@ -34,7 +34,7 @@ def test_brute_force_minimal_tile_size(t_max, step):
 
 
 def test_variant_choice_mirrors_the_library():
-    # the choice without a device to ask (no split-K, fixed 192-row
+    # the choice without a device to ask (no split-K, fixed 256-row
     # boundary); with a device the GPU test of the split-K choice compares
     # the mirror with the device's answers
     import torch
@@ -43,7 +43,7 @@ def test_variant_choice_mirrors_the_library():
         pytest.skip("a device is present: the library's choice depends on it")
     for E in (1, 4, 12, 32, 100, 512):
         for N in (256, 3584, 4096, 6144):
-            for rows in (0, 1, 16, 48 * E, 48 * E + E, 192 * E, 192 * E + E, 640 * E, 131072):
+            for rows in (0, 1, 16, 48 * E, 48 * E + E, 256 * E, 256 * E + E, 640 * E, 131072):
                 v = T.pick_variant(E, N, rows)
                 assert hg.hg_gemm_token_tile(E, N, 6144, rows) == T.VARIANT_T_MAX[v], (E, N, rows)
 
@@ -56,39 +56,43 @@ def test_forced_variant_token_tiles():
         assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 112
         hg.hg_set_gemm_variant(4)
         assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 224
-        assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 224   # falls back to variant 3
-        hg.hg_set_gemm_variant(5)
-        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 96
-        assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 112   # falls back to variant 2
-        hg.hg_set_gemm_variant(7)
-        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 112
-        assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 112   # falls back to variant 2
+        assert hg.hg_gemm_token_tile(32, 384, 6144, 10) == 224   # falls back to variant 8
+        hg.hg_set_gemm_variant(1)
+        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 64
+        hg.hg_set_gemm_variant(6)
+        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 32
+        hg.hg_set_gemm_variant(8)
+        assert hg.hg_gemm_token_tile(32, 4096, 6144, 10) == 224
     finally:
         hg.hg_set_gemm_variant(prev)
-    with pytest.raises(ValueError):
-        hg.hg_set_gemm_variant(9)
+    for removed in (3, 5, 7, 9, -1):
+        with pytest.raises(ValueError):
+            hg.hg_set_gemm_variant(removed)
 
 
 @pytest.mark.parametrize("E,N,K,rows,want", [
     (12, 6144, 3584, 1024, 2),    # 85 rows per expert: one 112-row tile each, same units
-    (12, 6144, 3584, 1408, 8),    # 117: two 112-row tiles or one 224-row tile, 4 rounds vs 2
-    (12, 6144, 3584, 1792, 8),
-    (12, 6144, 3584, 2048, 8),    # 170 rows per expert: model 0.854 (measured 12 % faster)
+    (12, 6144, 3584, 1408, 4),    # 117: two 112-row tiles or one 224-row tile, 4 rounds vs 2
+    (12, 6144, 3584, 1792, 4),
+    (12, 6144, 3584, 2048, 4),    # 170 rows per expert: model 0.854 (measured 7.5 % faster)
     (32, 6144, 2048, 4096, 2),    # 128 rows per expert on the down shape: model 0.863 stays
     (12, 3584, 3072, 1792, 2),    # 336 units of 224 rows fill 1.1 waves: the 2nd round is wasted
-    (12, 3584, 3072, 2560, 2),    # above 192 rows, still variant 2 (3 rounds vs 2 costlier ones)
-    (12, 6144, 3584, 2560, 8),
+    (12, 3584, 3072, 2560, 2),    # 213 rows: no predicted gain of 14 %
+    (12, 6144, 3584, 2560, 2),
     (32, 4096, 6144, 4096, 2),    # 128 rows per expert: 7 rounds vs 4 at 1.58x, below the margin
-    (32, 6144, 2048, 6144, 2),
-    (32, 4096, 6144, 9216, 8),
-    (32, 4096, 6144, 16384, 8),
-    (32, 6144, 2048, 131072, 8),
+    (32, 6144, 2048, 6144, 2),    # 192 rows (gate/up M = 768 measured 9 % faster on variant 2)
+    (32, 6144, 2048, 8192, 2),    # 256 rows (down M = 1024 measured 4 % faster on variant 2)
+    (32, 4096, 6144, 9216, 4),    # 288 rows: above 256, the CTA-pair variant
+    (32, 4096, 6144, 16384, 4),
+    (32, 6144, 2048, 131072, 4),
+    (32, 384, 2048, 131072, 8),   # N % 256 != 0: 224-row tiles on single CTAs
 ])
 def test_wave_model_variant_choice(E, N, K, rows, want):
-    # with a device of 152 SMs the mean-rows default moves only where the
-    # wave model predicts a 14-15 % gain; without a device it never moves
+    # with a device of 152 SMs the wave model can move shapes of at most
+    # 256 rows per expert to the large tile; without a device it never does
     assert T.pick_variant(E, N, rows, K, num_sms=152, split_ctas=296) == want
-    assert T.pick_variant(E, N, rows, K) == (2 if rows // E <= 192 else 8)
+    large = 4 if N % 256 == 0 else 8
+    assert T.pick_variant(E, N, rows, K) == (2 if rows // E <= 256 else large)
 
 
 def test_tile_inflation_vs_fixed_128():
