@@ -263,6 +263,13 @@ int32_t hg_set_gemm_variant(int32_t variant);
  *   sorted_to_src  int32 [M*top_k] from hg_plan_expert_offsets.
  *   a_fp8          uint8 [M*top_k, K] out, 16-byte aligned; a_scale uint8 [M*top_k, K/128] out.
  * K % 128 == 0.  One kernel on `stream`; no host synchronisation.
+ *
+ * This is the slow form: organised per sorted row, it reads and quantises
+ * every token top_k times, and the quantisation arithmetic, not memory,
+ * bounds it (about 0.24 of HBM bandwidth at top_k = 8, M = 2048, K = 6144,
+ * against about 0.70 for hg_quantize_scatter_acts, which writes the same
+ * bytes).  Prefer hg_quantize_scatter_acts; this form serves callers that
+ * hold only sorted_to_src.
  */
 hg_status hg_quantize_gather_acts(const uint16_t* x_bf16, int32_t M, int32_t K, int32_t top_k,
                                   const int32_t* sorted_to_src, uint8_t* a_fp8,
