@@ -83,8 +83,12 @@ struct GemmCfg {
     static constexpr uint32_t kRxSlotBytes = 32 * T * 4;     // one lane quadrant, FP32
     static constexpr int kRxSlots = CL == 1 ? 0 : (CL == 2 ? 2 : 3);
     static constexpr uint32_t kRxBytes = kRxSlots * kRxSlotBytes;
-    // scale warps take the stages in turn: one per ring slot, at most four
-    static constexpr int kSfWarps = S < 4 ? S : 4;
+    // scale warps take the stages in turn: one per ring slot.  Each must own
+    // exactly one slot: its waits on the slot's empty barrier are parity
+    // waits, which are only exact for the phase right after the one it last
+    // waited for (a warp visiting a slot several ring revolutions apart could
+    // see an older phase of the same parity complete).
+    static constexpr int kSfWarps = S;
     static constexpr int kThreads = 32 * (6 + kSfWarps);   // TMA, MMA, 4 epilogue, scale warps
     static constexpr uint32_t kATileBytes = T * kBK;
     static constexpr int kSfbAtoms = T > 128 ? 2 : 1;      // 128 tokens per scale block
@@ -107,6 +111,7 @@ struct GemmCfg {
     static constexpr size_t kSmemBudget =
         C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
     static_assert(CL == 1 || CL == 2 || CL == 4, "split over 2 or 4 CTAs");
+    static_assert(S <= 4, "scale warps 2, 3, 8, 9: one per ring slot");
     static_assert(AB == 2 || (AB == 1 && CL == 1), "one accumulator buffer, without split-K");
     static_assert(8 * (3 * S + 5 + 8) <= 256, "barrier area");
     // experts whose scheduler tables still fit next to the ring (<= kMaxE)
@@ -132,7 +137,7 @@ struct PairCfg {
     static constexpr int kHalf = T / 2;
     static constexpr int kStages = S;
     static constexpr int kCtasPerSm = C;
-    static constexpr int kSfWarps = S;
+    static constexpr int kSfWarps = S;      // one per ring slot (see GemmCfg)
     static constexpr int kThreads = 32 * (6 + S);
     static constexpr uint32_t kATileBytes = kHalf * kBK;
     static constexpr int kSfbAtoms = T > 128 ? 2 : 1;

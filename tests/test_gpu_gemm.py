@@ -455,3 +455,42 @@ def test_random_problems_every_variant(cuda_lib, seed):
     finally:
         cuda_lib.hg_set_gemm_variant(prev)
     assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def test_tensor_map_cache_same_address_other_shapes(cuda_lib):
+    # Encoded tensor maps are cached by (address, shape).  One activation
+    # buffer and one weight buffer are reused at the same addresses with other
+    # row counts, expert counts and K, and then more distinct buffers than the
+    # cache holds are used before the first shape comes back; every call must
+    # match the oracle.
+    rng = np.random.default_rng(21)
+    a_buf = torch.empty(300 * 2048, dtype=torch.uint8, device="cuda")
+    w_buf = torch.empty(4 * 256 * 1024, dtype=torch.uint8, device="cuda")
+
+    def run(E, N, K, cuts, seed):
+        r = np.random.default_rng(seed)
+        R = cuts[-1]
+        a, a_s, w, w_s = _rand_codes(r, R, K, E, N)
+        av = a_buf[:R * K].view(R, K)
+        av.copy_(torch.from_numpy(a))
+        wv = w_buf[:E * N * K // 2].view(E, N, K // 2)
+        wv.copy_(torch.from_numpy(w))
+        out = _run_gemm(cuda_lib, av, a_s, wv, w_s, cuts)
+        ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K)
+        assert_rows_close(bf16_bits(out), ref, f"cache E={E} N={N} K={K} R={R}")
+
+    shapes = [(3, 256, 1024, [0, 40, 41, 200]), (2, 256, 1024, [0, 150, 300]),
+              (4, 128, 2048, [0, 10, 90, 91, 250]), (3, 256, 512, [0, 1, 2, 3])]
+    for i, sh in enumerate(shapes):
+        run(*sh, seed=100 + i)
+        run(*sh, seed=150 + i)      # same address and shape: a cache hit, new contents
+    # more distinct activation buffers than the 16 cached entries
+    for i in range(20):
+        E, N, K, cuts = 1, 128, 512, [0, 16 + i]
+        r = np.random.default_rng(200 + i)
+        a, a_s, w, w_s = _rand_codes(r, cuts[-1], K, E, N)
+        out = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
+        assert_rows_close(bf16_bits(out), G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K),
+                          f"distinct buffer {i}")
+    run(*shapes[0], seed=100)
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
