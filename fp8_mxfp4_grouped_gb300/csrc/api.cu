@@ -97,10 +97,17 @@ struct AMapEntry {
     int32_t rows = 0, K = 0;
     AMaps maps;
 };
+struct OMapEntry {
+    const void* p = nullptr;
+    int32_t rows = 0, N = 0;
+    CUtensorMap map;
+};
 WMapEntry g_wmap[kMapCacheEntries];
 AMapEntry g_amap[kMapCacheEntries];
+OMapEntry g_omap[kMapCacheEntries];
 int g_wmap_next = 0;
 int g_amap_next = 0;
+int g_omap_next = 0;
 std::mutex g_map_mu;
 
 void map_cache_reset() {
@@ -108,8 +115,9 @@ void map_cache_reset() {
     for (int i = 0; i < kMapCacheEntries; ++i) {
         g_wmap[i].p = nullptr;
         g_amap[i].p = nullptr;
+        g_omap[i].p = nullptr;
     }
-    g_wmap_next = g_amap_next = 0;
+    g_wmap_next = g_amap_next = g_omap_next = 0;
 }
 
 // Weights: [E*N rows, K elements] of E2M1, unpacked by the TMA into one
@@ -181,6 +189,36 @@ int plan_nblk(long long R) {
     if (n < 1) n = 1;
     if (n > kPlanMaxBlocks) n = kPlanMaxBlocks;
     return static_cast<int>(n);
+}
+
+// Output: [rows, N] BF16 (as 16-bit words), no swizzle, boxes of 16 rows x
+// 32 columns, for the epilogues that write whole 16-row chunks with TMA
+// stores.
+hg_status out_map(PFN_cuTensorMapEncodeTiled_v12000 encode, uint16_t* out, int32_t rows,
+                  int32_t N, CUtensorMap* map) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < kMapCacheEntries; ++i) {
+        const OMapEntry& c = g_omap[i];
+        if (c.p == out && c.rows == rows && c.N == N) {
+            *map = c.map;
+            return HG_OK;
+        }
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    cuuint32_t box[2] = {32, 16};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, out, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return HG_ERR_CUDA;
+    OMapEntry& slot = g_omap[g_omap_next];
+    g_omap_next = (g_omap_next + 1) % kMapCacheEntries;
+    slot.p = out;
+    slot.rows = rows;
+    slot.N = N;
+    slot.map = *map;
+    return HG_OK;
 }
 
 }  // namespace
@@ -336,7 +374,17 @@ hg_status grouped_gemm(const uint8_t* a_fp8, const uint8_t* a_scale, bool a_scal
     a.timeout_ns = g_timeout_ns.load();
     a.num_sms = d->num_sms;
     a.variant = variant;
-    return launch_grouped_gemm(a, map_w, map_a, reinterpret_cast<cudaStream_t>(stream)) ==
+    // The CTA-pair kernel writes whole 16-row chunks of its output tile with
+    // TMA stores when the output is 16-byte aligned (the tensor map's base
+    // address rule); ragged chunks and unaligned outputs use plain stores.
+    CUtensorMap map_o;
+    const CUtensorMap* map_o_ptr = nullptr;
+    if (variant == 4 && aligned(out_bf16, 16)) {
+        st = out_map(encode, out_bf16, rows, N, &map_o);
+        if (st != HG_OK) return st;
+        map_o_ptr = &map_o;
+    }
+    return launch_grouped_gemm(a, map_w, map_a, map_o_ptr, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? HG_OK
                : HG_ERR_CUDA;

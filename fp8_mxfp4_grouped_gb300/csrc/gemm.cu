@@ -150,7 +150,10 @@ struct PairCfg {
     static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
     static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
     static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;
-    static constexpr uint32_t kOffBar = kOffSfb + S * kSfbBytes;
+    // output staging: per epilogue warp two 16-row x 32-column BF16 buffers
+    static constexpr uint32_t kOutChunkBytes = 16 * 32 * 2;
+    static constexpr uint32_t kOffOut = kOffSfb + S * kSfbBytes;
+    static constexpr uint32_t kOffBar = kOffOut + kEpiWarps * 2 * kOutChunkBytes;
     static constexpr uint32_t kOffMisc = kOffBar + 256;
     static constexpr uint32_t kOffSched = kOffMisc + 64;
     static constexpr size_t smem_bytes(int E) {
@@ -732,6 +735,7 @@ template <class Cfg>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
 grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                          const __grid_constant__ AMaps map_a,
+                         const __grid_constant__ CUtensorMap map_out, int out_tma,
                          const uint8_t* __restrict__ a_scale, const uint8_t* __restrict__ w_scale,
                          const int32_t* __restrict__ offsets, int E, int N, int K, int rows,
                          int as_rs, int as_ks, uint16_t* __restrict__ out, uint32_t* status,
@@ -965,6 +969,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         // ---------------------------------------------------- epilogue --
         const int q = warp & 3;
         const uint32_t tempty_leader = ptx::mapa_shared(bar_tempty, 0);
+        const uint32_t out_stage = sbase + Cfg::kOffOut + q * 2 * Cfg::kOutChunkBytes;
+        uint32_t out_chunk = 0;
         uint32_t tc = 0;
         for (int u = static_cast<int>(blockIdx.x >> 1); u < U;
              u += static_cast<int>(gridDim.x >> 1), ++tc) {
@@ -973,19 +979,40 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
             const uint32_t b = tc & 1u;
             if (!wait_bounded<true>(bar_tfull + 8 * b, (tc >> 1) & 1u, wctx, kRoleEpilogue, b)) break;
             ptx::tc_fence_after();
-            const int n = wrow0 + static_cast<int>(rank) * kBW + 32 * q + lane;
-            uint16_t* dst = out + static_cast<size_t>(row0) * N + n;
+            const int n_warp = wrow0 + static_cast<int>(rank) * kBW + 32 * q;   // warp's first column
+            uint16_t* dst = out + static_cast<size_t>(row0) * N + n_warp + lane;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * Cfg::kAccCols;
             for (int c0 = 0; c0 < nrows; c0 += 16) {
                 uint32_t v[16];
                 ptx::tmem_ld_32x32b_x16(taddr + c0, v);
                 ptx::tmem_ld_wait();
+                if (out_tma && c0 + 16 <= nrows) {
+                    // 16 whole rows x this warp's 32 columns: staged in shared
+                    // memory and written by one TMA store (rows past the
+                    // expert's last row never take this path)
+                    const uint32_t buf = out_stage + (out_chunk & 1u) * Cfg::kOutChunkBytes;
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();   // this buffer's last store has read it
+                    __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (c0 + j < nrows) {
-                        dst[static_cast<size_t>(c0 + j) * N] =
-                            __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                    for (int j = 0; j < 16; ++j) {
+                        ptx::sts_u16(buf + j * 64 + lane * 2,
+                                     __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j]))));
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&map_out, buf, n_warp, row0 + c0);
+                        ptx::bulk_commit_group();
+                    }
+                    ++out_chunk;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (c0 + j < nrows) {
+                            dst[static_cast<size_t>(c0 + j) * N] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+                        }
                     }
                 }
             }
@@ -993,6 +1020,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_remote(tempty_leader + 8 * b);
         }
+        // every staged store has completed before the CTA can exit
+        if (lane == 0) ptx::bulk_wait_group_all();
+        __syncwarp();
     } else {
         // ------------------------------------------- scale staging -----
         // Weight scales of this CTA's 128 rows; token scales of the WHOLE
@@ -1273,13 +1303,13 @@ cudaError_t launch_cluster(const GemmArgs& a, const CUtensorMap& map_w, const AM
 
 template <class Cfg>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
-                        cudaStream_t stream) {
+                        const CUtensorMap* map_out, cudaStream_t stream) {
     const long long grid = grid_pair<Cfg>(a);
     if (grid < 2) return cudaSuccess;
     grouped_w4a8_pair_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
                                     stream>>>(
-        map_w, map_a, a.a_scale, a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs,
-        a.as_ks, a.out, a.status, a.timeout_ns);
+        map_w, map_a, map_out ? *map_out : map_w, map_out ? 1 : 0, a.a_scale, a.w_scale,
+        a.offsets, a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out, a.status, a.timeout_ns);
     return cudaGetLastError();
 }
 
@@ -1398,11 +1428,11 @@ long long gemm_launch_ctas(const GemmArgs& a) {
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
-                                cudaStream_t stream) {
+                                const CUtensorMap* map_out, cudaStream_t stream) {
     switch (a.variant) {
         case 1: return launch_cfg<CfgSmall>(a, map_w, map_a, stream);
         case 2: return launch_cfg<CfgMid>(a, map_w, map_a, stream);
-        case 4: return launch_pair<CfgPair>(a, map_w, map_a, stream);
+        case 4: return launch_pair<CfgPair>(a, map_w, map_a, map_out, stream);
         case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, stream);
         default: return launch_cfg<CfgWide2>(a, map_w, map_a, stream);
     }

@@ -82,7 +82,7 @@ struct GemmArgs {
     uint32_t* status;
     uint64_t timeout_ns;
     int num_sms;
-    int variant;   // 1 small tiles / 2 CTAs per SM, 2 mid, 3 large tiles / 1 CTA per SM, 4 CTA pairs
+    int variant;   // 1, 2, 4 (CTA pairs), 6 (split-K), 8: see hg_set_gemm_variant
 };
 
 // Lanes of the warp whose key equals this lane's, for keys in [0, 2^nbits)
@@ -107,8 +107,11 @@ struct AMaps {
     CUtensorMap box[4];
 };
 
+// map_out: the output [rows, N] BF16 with boxes of 16 rows x 32 columns, for
+// kernels that write whole 16-row chunks with TMA stores; nullptr: plain
+// stores only.
 cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
-                                cudaStream_t stream);
+                                const CUtensorMap* map_out, cudaStream_t stream);
 size_t gemm_smem_bytes(int variant, int32_t E);
 long long gemm_launch_ctas(const GemmArgs& a);   // CTAs the launch would use
 int gemm_max_experts();
