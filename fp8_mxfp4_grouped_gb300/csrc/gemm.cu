@@ -21,7 +21,9 @@
 //    128/64/32/16 rows; both with the L2 evict-last hint; no multicast);
 //    up to four scale warps (2, 3, 8, 9) stage the block scales into the
 //    tensor core's scale layout (activation scales are per 128-K, replicated
-//    into the four 32-K blocks they cover); warp 1 copies scales to TMEM and
+//    into the four 32-K blocks they cover; the CTA-pair kernel instead packs
+//    four stages' activation scales into one scale word, staged by a warp of
+//    its own, and picks the byte with the MMA's scale-factor id); warp 1 copies scales to TMEM and
 //    issues tcgen05.mma kind::mxf8f6f4 with block scaling, accumulating FP32
 //    in TMEM; warps 4..7 drain the TMEM accumulator to BF16 with stores cut
 //    at the expert's last row (two accumulator buffers, or one where two
@@ -131,6 +133,12 @@ struct GemmCfg {
 // multiple of 32, split in halves between the two CTAs); S: ring stages.
 // Each CTA holds its 128 weight rows and half of the token tile per stage, so
 // a pair computes a 256 x T tile with one MMA instruction stream.
+// Token scales travel in groups of kSfbGroup stages: an activation scale
+// covers a whole 128-K stage, so the four bytes of a TMEM scale word, which
+// the MMA selects by its B scale-factor id, can carry four stages' scales of
+// one token instead of one stage's scale four times.  One copy to TMEM per
+// group then replaces one per stage (the per-stage token-scale copies of
+// CTA pairs measured 6-7 % of the launch at large M on GB300).
 template <int T, int S, int C>
 struct PairCfg {
     static constexpr int kTMax = T;
@@ -138,21 +146,24 @@ struct PairCfg {
     static constexpr int kStages = S;
     static constexpr int kCtasPerSm = C;
     static constexpr int kSfWarps = S;      // one per ring slot (see GemmCfg)
-    static constexpr int kThreads = 32 * (6 + S);
+    static constexpr int kSfbWarp = 6 + S;  // token scales, one group at a time
+    static constexpr int kThreads = 32 * (7 + S);
+    static constexpr int kSfbGroup = 4;     // stages per token-scale group
+    static constexpr int kSfbSlots = 3;     // token-scale groups in flight
     static constexpr uint32_t kATileBytes = kHalf * kBK;
     static constexpr int kSfbAtoms = T > 128 ? 2 : 1;
     static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
     static constexpr uint32_t kAccCols = T;
     static constexpr uint32_t kTmemCols = 512 / C;
-    static constexpr uint32_t kSfCol0 = 2 * kAccCols;
-    static constexpr uint32_t kSfSlotCols = 4 + 4 * kSfbAtoms;
+    static constexpr uint32_t kSfCol0 = 2 * kAccCols;       // weight scales: 4 columns per ring slot
+    static constexpr uint32_t kSfbCol0 = kSfCol0 + 4 * S;   // token scales: 4 per atom per group slot
     static constexpr uint32_t kOffW = 0;
     static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
     static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
-    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;
+    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;   // [group slot] token scales
     // output staging: per epilogue warp two 16-row x 32-column BF16 buffers
     static constexpr uint32_t kOutChunkBytes = 16 * 32 * 2;
-    static constexpr uint32_t kOffOut = kOffSfb + S * kSfbBytes;
+    static constexpr uint32_t kOffOut = kOffSfb + kSfbSlots * kSfbBytes;
     static constexpr uint32_t kOffBar = kOffOut + kEpiWarps * 2 * kOutChunkBytes;
     static constexpr uint32_t kOffMisc = kOffBar + 256;
     static constexpr uint32_t kOffSched = kOffMisc + 64;
@@ -163,10 +174,11 @@ struct PairCfg {
         C == 1 ? kSmemPerBlockMax : kSmemPerSm / C - kSmemReservedPerBlock;
     static_assert(T % 32 == 0 && T >= 32 && T <= 256, "MMA N, split in two halves of 16k");
     static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
-    static_assert(kSfCol0 + S * kSfSlotCols <= kTmemCols, "TMEM budget");
+    static_assert(kSfbCol0 + kSfbSlots * 4 * kSfbAtoms <= kTmemCols, "TMEM budget");
     static_assert(smem_bytes(kMaxE) <= kSmemBudget, "shared memory budget");
-    static_assert(8 * (3 * S + 5) <= 256, "barrier area");
-    static_assert(C * 32 * (6 + S) * 96 <= 65536, "registers for C resident CTAs");
+    static_assert(8 * (3 * S + 5 + 2 * kSfbSlots) <= 256, "barrier area");
+    static_assert(C * kThreads * 96 <= 65536, "registers for C resident CTAs");
+    static_assert(kSfbGroup == 4, "four stages per 32-bit scale word");
 };
 
 using CfgPair = PairCfg<224, 5, 1>;     // many rows per expert, N % 256 == 0
@@ -762,6 +774,10 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     const uint32_t bar_tfull = bar_empty + 8 * kStages;
     const uint32_t bar_tempty = bar_tfull + 16;               // leader: both CTAs drained TMEM
     const uint32_t bar_done = bar_tempty + 16;
+    // token-scale groups: full (leader, one arrival per CTA), empty (both
+    // CTAs, the leader's multicast commit after the group's last MMA)
+    const uint32_t bar_sfb_full = bar_done + 8;
+    const uint32_t bar_sfb_empty = bar_sfb_full + 8 * Cfg::kSfbSlots;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(base + Cfg::kOffMisc);
     int32_t* s_start = reinterpret_cast<int32_t*>(base + Cfg::kOffSched);
     int32_t* s_rows = s_start + E;
@@ -780,6 +796,10 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
             ptx::mbar_init(bar_tempty + 8 * b, 2 * kEpiWarps);
         }
         ptx::mbar_init(bar_done, 1);
+        for (int s = 0; s < Cfg::kSfbSlots; ++s) {
+            ptx::mbar_init(bar_sfb_full + 8 * s, 2);
+            ptx::mbar_init(bar_sfb_empty + 8 * s, 1);
+        }
         misc[1] = 0u;   // abort flag
         ptx::fence_barrier_init();
     }
@@ -909,7 +929,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         if (leader) {
             // --------------------------------------- MMA issuer (pair) ---
             // Whole converged warp of the even CTA; the elected lane issues.
-            uint32_t g = 0, tc = 0;
+            uint32_t g = 0, tc = 0, gr = 0;   // stages, units, token-scale groups
             bool ok = true;
             for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
                  u += static_cast<int>(gridDim.x >> 1), ++tc) {
@@ -925,9 +945,29 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 const uint32_t idesc0 =
                     ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, 2 * kBW, n_mma);
                 const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
+                uint32_t gslot = 0, sfb_col = 0;
                 for (int ks = 0; ks < KT; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
+                    if ((ks & (Cfg::kSfbGroup - 1)) == 0) {
+                        // a new token-scale group: both CTAs' words to TMEM
+                        gslot = gr % Cfg::kSfbSlots;
+                        if (!__all_sync(0xFFFFFFFFu,
+                                        wait_bounded<true>(bar_sfb_full + 8 * gslot,
+                                                           (gr / Cfg::kSfbSlots) & 1u, wctx,
+                                                           kRoleMma, 0x20u | gslot))) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        sfb_col = tmem_base + Cfg::kSfbCol0 + gslot * 4 * Cfg::kSfbAtoms;
+                        const uint32_t sfb = sbase + Cfg::kOffSfb + gslot * Cfg::kSfbBytes;
+                        ptx::tc_cp_32x128b_warpx4_pair_elect(sfb_col, ptx::desc_sf_32x16(sfb));
+                        if (Cfg::kSfbAtoms > 1 && n_mma > 128) {
+                            ptx::tc_cp_32x128b_warpx4_pair_elect(sfb_col + 4,
+                                                                 ptx::desc_sf_32x16(sfb + 512));
+                        }
+                    }
                     const bool ready =
                         wait_bounded<true>(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) &&
                         wait_bounded<true>(bar_full_sf + 8 * slot, ph, wctx, kRoleMma,
@@ -937,26 +977,26 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * Cfg::kSfSlotCols;
+                    const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * 4;
                     const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
-                    const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
                     ptx::tc_cp_32x128b_warpx4_pair_elect(sf_col, ptx::desc_sf_32x16(sfa));
-                    ptx::tc_cp_32x128b_warpx4_pair_elect(sf_col + 4, ptx::desc_sf_32x16(sfb));
-                    if (Cfg::kSfbAtoms > 1 && n_mma > 128) {
-                        ptx::tc_cp_32x128b_warpx4_pair_elect(sf_col + 8,
-                                                             ptx::desc_sf_32x16(sfb + 512));
-                    }
                     const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
                     const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
+                    const uint32_t b_id = static_cast<uint32_t>(ks) & (Cfg::kSfbGroup - 1);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk) {
                         ptx::mma_mxf8f6f4_1x_pair_elect(
                             d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
                             ptx::desc_kmajor_sw128(asm_ + kk * 32),
-                            ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col, sf_col + 4,
+                            ptx::idesc_with_sf_ids(idesc0, kk, b_id), sf_col, sfb_col,
                             (ks | kk) != 0 ? 1u : 0u);
                     }
                     ptx::tc_commit_pair_multicast_elect(bar_empty + 8 * slot, 0x3);
+                    if (b_id == Cfg::kSfbGroup - 1 || ks == KT - 1) {
+                        // the group's last MMA: its buffer and TMEM columns free once done
+                        ptx::tc_commit_pair_multicast_elect(bar_sfb_empty + 8 * gslot, 0x3);
+                        ++gr;
+                    }
                 }
                 if (!ok) break;
                 ptx::tc_commit_pair_multicast_elect(bar_tfull + 8 * b, 0x3);
@@ -1023,10 +1063,77 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         // every staged store has completed before the CTA can exit
         if (lane == 0) ptx::bulk_wait_group_all();
         __syncwarp();
+    } else if (warp == Cfg::kSfbWarp) {
+        // ------------------------------------- token-scale staging -----
+        // One group of kSfbGroup stages of a unit at a time: word c of lane l
+        // holds the scales of token 128a + l + 32c (atom a) at the group's
+        // stages, byte j for stage 4m + j (bytes past the unit's last stage,
+        // and tokens past the tile, hold 1.0).  Each CTA's TMEM needs the
+        // scales of the WHOLE token tile; both CTAs arrive on the leader's
+        // group barrier.
+        const uint32_t sfb_full_leader = ptx::mapa_shared(bar_sfb_full, 0);
+        const bool word_loads = as_ks == 1 && (as_rs & 3) == 0 && (KT & 3) == 0 &&
+                                (reinterpret_cast<uintptr_t>(a_scale) & 3u) == 0;
+        uint32_t gr = 0;
+        bool ok = true;
+        for (int u = static_cast<int>(blockIdx.x >> 1); ok && u < U;
+             u += static_cast<int>(gridDim.x >> 1)) {
+            int e, wrow0, row0, nrows, n_mma;
+            unit_of(u, e, wrow0, row0, nrows, n_mma);
+            for (int k4 = 0; k4 < KT; k4 += Cfg::kSfbGroup, ++gr) {
+                const uint32_t gslot = gr % Cfg::kSfbSlots;
+                const int nst = min(Cfg::kSfbGroup, KT - k4);
+                uint32_t av[4 * Cfg::kSfbAtoms];
+#pragma unroll
+                for (int i = 0; i < 4 * Cfg::kSfbAtoms; ++i) {
+                    const int tok = 128 * (i >> 2) + lane + 32 * (i & 3);
+                    const int r = row0 + tok;
+                    uint32_t v = 0x7F7F7F7Fu;
+                    if (tok < n_mma && r < rows) {
+                        const uint8_t* src = a_scale + static_cast<size_t>(r) * as_rs +
+                                             static_cast<size_t>(k4) * as_ks;
+                        if (word_loads) {
+                            v = __ldg(reinterpret_cast<const uint32_t*>(src));   // 4 whole stages
+                        } else {
+                            v = 0u;
+#pragma unroll
+                            for (int j = 0; j < Cfg::kSfbGroup; ++j) {
+                                const uint32_t byte =
+                                    j < nst ? __ldg(src + static_cast<size_t>(j) * as_ks) : 0x7Fu;
+                                v |= byte << (8 * j);
+                            }
+                        }
+                    }
+                    av[i] = v;
+                }
+                if (!__all_sync(0xFFFFFFFFu,
+                                wait_bounded<true>(bar_sfb_empty + 8 * gslot,
+                                                   ((gr / Cfg::kSfbSlots) & 1u) ^ 1u, wctx,
+                                                   kRoleScale, 0x40u | gslot))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sfb = sbase + Cfg::kOffSfb + gslot * Cfg::kSfbBytes + 16 * lane;
+                sts_v4(sfb, av[0], av[1], av[2], av[3]);
+                if (Cfg::kSfbAtoms > 1 && n_mma > 128) {
+                    sts_v4(sfb + 512, av[4 % (4 * Cfg::kSfbAtoms)], av[5 % (4 * Cfg::kSfbAtoms)],
+                           av[6 % (4 * Cfg::kSfbAtoms)], av[7 % (4 * Cfg::kSfbAtoms)]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader) {
+                        ptx::mbar_arrive(bar_sfb_full + 8 * gslot);
+                    } else {
+                        ptx::mbar_arrive_remote(sfb_full_leader + 8 * gslot);
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------------------- scale staging -----
-        // Weight scales of this CTA's 128 rows; token scales of the WHOLE
-        // token tile (each CTA's TMEM needs all N columns' scales).
+        // Weight scales of this CTA's 128 rows, one stage per warp in turn
+        // (token scales: the token-scale warp above).
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;
         const int ws_row = K / 32;
         const uint32_t full_sf_leader = ptx::mapa_shared(bar_full_sf, 0);
@@ -1050,19 +1157,6 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 for (int c = 0; c < 4; ++c) {
                     wv[c] = ldg_u32(wsrc + static_cast<size_t>(32 * c) * ws_row + ks * 4);
                 }
-                uint32_t av[4 * Cfg::kSfbAtoms];
-#pragma unroll
-                for (int i = 0; i < 4 * Cfg::kSfbAtoms; ++i) {
-                    const int tok = 128 * (i >> 2) + lane + 32 * (i & 3);
-                    const int r = row0 + tok;
-                    av[i] = 0x7F7F7F7Fu;
-                    if (tok < n_mma && r < rows) {
-                        av[i] = static_cast<uint32_t>(
-                                    __ldg(a_scale + static_cast<size_t>(r) * as_rs +
-                                          static_cast<size_t>(ks) * as_ks)) *
-                                0x01010101u;
-                    }
-                }
                 if (!__all_sync(0xFFFFFFFFu, wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx,
                                                                 kRoleScale, slot))) {
                     ok = false;
@@ -1074,13 +1168,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                                         ks * kBK, row0 + static_cast<int>(rank) * (n_mma / 2),
                                         n_mma / 2, full_tma_leader + 8 * slot, pol_a);
                 const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes + 16 * lane;
-                const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes + 16 * lane;
                 sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
-                sts_v4(sfb, av[0], av[1], av[2], av[3]);
-                if (Cfg::kSfbAtoms > 1 && n_mma > 128) {
-                    sts_v4(sfb + 512, av[4 % (4 * Cfg::kSfbAtoms)], av[5 % (4 * Cfg::kSfbAtoms)],
-                           av[6 % (4 * Cfg::kSfbAtoms)], av[7 % (4 * Cfg::kSfbAtoms)]);
-                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

@@ -381,7 +381,10 @@ def test_graph_capture_replay_matches_eager(cuda_lib):
 # ----------------------------------------------------- M-major activation scales --
 
 @pytest.mark.parametrize("E,N,K,cuts", [(6, 384, 1024, [0, 1, 17, 17, 240, 470, 700]),
-                                        (2, 512, 3072, [0, 129, 260])])
+                                        (2, 512, 3072, [0, 129, 260]),
+                                        # 9 stages: CTA pairs stage token scales in groups of
+                                        # four, the last group partial
+                                        (3, 512, 1152, [0, 100, 100, 333])])
 def test_mmajor_scales_ragged(cuda_lib, variant, E, N, K, cuts):
     rng = np.random.default_rng(E * 77 + K)
     R = cuts[-1]
@@ -395,9 +398,10 @@ def test_mmajor_scales_ragged(cuda_lib, variant, E, N, K, cuts):
     assert_rows_close(bf16_bits(out), ref, f"m-major E={E} N={N} K={K}")
 
 
-@pytest.mark.parametrize("cid,M", [(1, 512), (2, 64)])
+@pytest.mark.parametrize("cid,M", [(1, 512), (2, 64), (1, 2048)])
 def test_mmajor_matches_row_major_full_size(cuda_lib, cid, M):
     # same codes, scales transposed: the two entry points must agree bit for bit
+    # (at M = 2048, CTA pairs: whole-word token-scale loads against byte loads)
     c = make_case(cid, M, device="cuda")
     off, _, _ = cuda_lib.hg_plan_expert_offsets(torch.from_numpy(c.topk_ids).cuda(), c.E)
     o_row = cuda_lib.hg_grouped_w4a8_gemm(c.a_fp8, c.a_scale, c.w_fp4, c.w_scale, off)
