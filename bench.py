@@ -93,20 +93,25 @@ def measured_traffic(M):
 
 def host_link_gbs(cs, dev):
     """Host<->device copy rates (GB/s) of this box with the largest batch's
-    pinned buffers: upload alone, download alone, and both at once (total)."""
+    pinned buffers: upload alone, download alone, and both at once (total);
+    each the best of five timed copies."""
     h = cs["host"]
     up_d = torch.empty_like(h["a"], device=dev)
     dn_d = torch.empty_like(h["out"], device=dev)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def timed(fn, reps=3):
+    def timed(fn, reps=5):
+        # best of single timed copies: an occasional slow one (see the
+        # end-to-end leg) must not lower the rate
         fn()
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
+        best = float("inf")
         for _ in range(reps):
+            t0 = time.perf_counter()
             fn()
-        torch.cuda.synchronize()
-        return (time.perf_counter() - t0) / reps
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
 
     def up():
         with torch.cuda.stream(s1):
