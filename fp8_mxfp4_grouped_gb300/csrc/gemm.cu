@@ -115,7 +115,7 @@ struct GemmCfg {
     static_assert(CL == 1 || CL == 2 || CL == 4, "split over 2 or 4 CTAs");
     static_assert(S <= 4, "scale warps 2, 3, 8, 9: one per ring slot");
     static_assert(AB == 2 || (AB == 1 && CL == 1), "one accumulator buffer, without split-K");
-    static_assert(8 * (3 * S + 5 + 8) <= 256, "barrier area");
+    static_assert(8 * (2 * S + 5 + 8) <= 256, "barrier area");
     // experts whose scheduler tables still fit next to the ring (<= kMaxE)
     static constexpr int kMaxExperts =
         (static_cast<long long>(kSmemBudget) - static_cast<long long>(smem_bytes(0))) / 20 < kMaxE
@@ -176,7 +176,7 @@ struct PairCfg {
     static_assert(kOffA % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms need 1024-B alignment");
     static_assert(kSfbCol0 + kSfbSlots * 4 * kSfbAtoms <= kTmemCols, "TMEM budget");
     static_assert(smem_bytes(kMaxE) <= kSmemBudget, "shared memory budget");
-    static_assert(8 * (3 * S + 5 + 2 * kSfbSlots) <= 256, "barrier area");
+    static_assert(8 * (2 * S + 5 + 2 * kSfbSlots) <= 256, "barrier area");
     static_assert(C * kThreads * 96 <= 65536, "registers for C resident CTAs");
     static_assert(kSfbGroup == 4, "four stages per 32-bit scale word");
 };
@@ -313,9 +313,11 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // bar_full_tma: a stage's tiles have landed (the producer's expect-tx
+    // arrival and the bytes) and its scales are staged (one arrival from the
+    // stage's scale warp), so the MMA warp waits on one barrier per stage.
     const uint32_t bar_full_tma = sbase + Cfg::kOffBar;
-    const uint32_t bar_full_sf = bar_full_tma + 8 * kStages;
-    const uint32_t bar_empty = bar_full_sf + 8 * kStages;
+    const uint32_t bar_empty = bar_full_tma + 8 * kStages;
     const uint32_t bar_tfull = bar_empty + 8 * kStages;
     const uint32_t bar_tempty = bar_tfull + 16;
     const uint32_t bar_done = bar_tempty + 16;
@@ -332,8 +334,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bar_full_tma + 8 * s, 1);
-            ptx::mbar_init(bar_full_sf + 8 * s, 1);
+            ptx::mbar_init(bar_full_tma + 8 * s, 2);
             ptx::mbar_init(bar_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -486,10 +487,8 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
             for (int ks = kCL > 1 ? k0 : 0; ks < (kCL > 1 ? k1 : KT); ++ks, ++g) {
                 const uint32_t slot = g % kStages;
                 const uint32_t ph = (g / kStages) & 1u;
-                const bool ready =
-                    wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) &&
-                    wait_bounded(bar_full_sf + 8 * slot, ph, wctx, kRoleMma, 0x10u | slot);
-                if (!__all_sync(0xFFFFFFFFu, ready)) {
+                if (!__all_sync(0xFFFFFFFFu,
+                                wait_bounded(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot))) {
                     ok = false;
                     break;
                 }
@@ -710,7 +709,7 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar_full_sf + 8 * slot);
+                if (lane == 0) ptx::mbar_arrive(bar_full_tma + 8 * slot);
             }
         }
         if (Cfg::kScaleWarpsLoadA && !ok) {
@@ -765,12 +764,12 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     const bool leader = rank == 0;
 
     // Leader (even CTA): bar_full_tma counts both CTAs' TMA bytes of a stage
-    // (the odd CTA's loads signal it directly), bar_full_sf takes one arrival
-    // from each CTA's scale warp.  bar_empty: in both CTAs, released by the
-    // leader's multicast commit.
+    // (the odd CTA's loads signal it directly) and takes one arrival from
+    // the leader's producer (with the expected bytes) and one from each
+    // CTA's scale warp, so the MMA warp waits on one barrier per stage.
+    // bar_empty: in both CTAs, released by the leader's multicast commit.
     const uint32_t bar_full_tma = sbase + Cfg::kOffBar;
-    const uint32_t bar_full_sf = bar_full_tma + 8 * kStages;
-    const uint32_t bar_empty = bar_full_sf + 8 * kStages;
+    const uint32_t bar_empty = bar_full_tma + 8 * kStages;
     const uint32_t bar_tfull = bar_empty + 8 * kStages;
     const uint32_t bar_tempty = bar_tfull + 16;               // leader: both CTAs drained TMEM
     const uint32_t bar_done = bar_tempty + 16;
@@ -787,8 +786,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bar_full_tma + 8 * s, 1);
-            ptx::mbar_init(bar_full_sf + 8 * s, 2);
+            ptx::mbar_init(bar_full_tma + 8 * s, 3);
             ptx::mbar_init(bar_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -968,11 +966,8 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                                                                  ptx::desc_sf_32x16(sfb + 512));
                         }
                     }
-                    const bool ready =
-                        wait_bounded<true>(bar_full_tma + 8 * slot, ph, wctx, kRoleMma, slot) &&
-                        wait_bounded<true>(bar_full_sf + 8 * slot, ph, wctx, kRoleMma,
-                                           0x10u | slot);
-                    if (!__all_sync(0xFFFFFFFFu, ready)) {
+                    if (!__all_sync(0xFFFFFFFFu, wait_bounded<true>(bar_full_tma + 8 * slot, ph,
+                                                                    wctx, kRoleMma, slot))) {
                         ok = false;
                         break;
                     }
@@ -1136,7 +1131,6 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         // (token scales: the token-scale warp above).
         const int sfw = (warp < 4) ? warp - 2 : warp - 8 + 2;
         const int ws_row = K / 32;
-        const uint32_t full_sf_leader = ptx::mapa_shared(bar_full_sf, 0);
         const uint32_t full_tma_leader = ptx::mapa_shared(bar_full_tma, 0);
         const uint64_t pol_a = ptx::policy_evict_last();
         uint32_t g = 0;
@@ -1173,9 +1167,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 __syncwarp();
                 if (lane == 0) {
                     if (leader) {
-                        ptx::mbar_arrive(bar_full_sf + 8 * slot);
+                        ptx::mbar_arrive(bar_full_tma + 8 * slot);
                     } else {
-                        ptx::mbar_arrive_remote(full_sf_leader + 8 * slot);
+                        ptx::mbar_arrive_remote(full_tma_leader + 8 * slot);
                     }
                 }
             }
