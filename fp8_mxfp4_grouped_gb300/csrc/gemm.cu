@@ -974,19 +974,17 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                     ptx::tc_fence_after();
                     const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * 4;
                     const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
-                    ptx::tc_cp_32x128b_warpx4_pair_elect(sf_col, ptx::desc_sf_32x16(sfa));
                     const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
                     const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
                     const uint32_t b_id = static_cast<uint32_t>(ks) & (Cfg::kSfbGroup - 1);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 32; ++kk) {
-                        ptx::mma_mxf8f6f4_1x_pair_elect(
-                            d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
-                            ptx::desc_kmajor_sw128(asm_ + kk * 32),
-                            ptx::idesc_with_sf_ids(idesc0, kk, b_id), sf_col, sfb_col,
-                            (ks | kk) != 0 ? 1u : 0u);
-                    }
-                    ptx::tc_commit_pair_multicast_elect(bar_empty + 8 * slot, 0x3);
+                    static_assert(kBK / 32 == 4, "four K = 32 MMAs per stage");
+                    ptx::pair_stage_elect(d_tmem, sf_col, ptx::desc_sf_32x16(sfa),
+                                          ptx::desc_kmajor_sw128(wsm), ptx::desc_kmajor_sw128(asm_),
+                                          ptx::idesc_with_sf_ids(idesc0, 0, b_id),
+                                          ptx::idesc_with_sf_ids(idesc0, 1, b_id),
+                                          ptx::idesc_with_sf_ids(idesc0, 2, b_id),
+                                          ptx::idesc_with_sf_ids(idesc0, 3, b_id), sfb_col,
+                                          ks != 0 ? 1u : 0u, bar_empty + 8 * slot, 0x3);
                     if (b_id == Cfg::kSfbGroup - 1 || ks == KT - 1) {
                         // the group's last MMA: its buffer and TMEM columns free once done
                         ptx::tc_commit_pair_multicast_elect(bar_sfb_empty + 8 * gslot, 0x3);
