@@ -498,22 +498,19 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
                 const uint32_t sfb_col = sf_col + 4;
                 const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
                 const uint32_t sfb = sbase + Cfg::kOffSfb + slot * Cfg::kSfbBytes;
-                ptx::tc_cp_32x128b_warpx4_elect(sf_col, ptx::desc_sf_32x16(sfa));
-                ptx::tc_cp_32x128b_warpx4_elect(sfb_col, ptx::desc_sf_32x16(sfb));
                 if (Cfg::kSfbAtoms > 1 && t.n_mma > 128) {
                     ptx::tc_cp_32x128b_warpx4_elect(sfb_col + 4, ptx::desc_sf_32x16(sfb + 512));
                 }
                 const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
                 const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBK / 32; ++kk) {
-                    ptx::mma_mxf8f6f4_1x_elect(d_tmem, ptx::desc_kmajor_sw128(wsm + kk * 32),
-                                               ptx::desc_kmajor_sw128(asm_ + kk * 32),
-                                               ptx::idesc_with_sf_ids(idesc0, kk, kk), sf_col,
-                                               sfb_col,
-                                               (ks != (kCL > 1 ? k0 : 0) || kk != 0) ? 1u : 0u);
-                }
-                ptx::tc_commit_elect(bar_empty + 8 * slot);
+                static_assert(kBK / 32 == 4, "four K = 32 MMAs per stage");
+                ptx::stage_elect(d_tmem, sf_col, ptx::desc_sf_32x16(sfa), sfb_col,
+                                 ptx::desc_sf_32x16(sfb), ptx::desc_kmajor_sw128(wsm),
+                                 ptx::desc_kmajor_sw128(asm_), ptx::idesc_with_sf_ids(idesc0, 0, 0),
+                                 ptx::idesc_with_sf_ids(idesc0, 1, 1),
+                                 ptx::idesc_with_sf_ids(idesc0, 2, 2),
+                                 ptx::idesc_with_sf_ids(idesc0, 3, 3),
+                                 ks != (kCL > 1 ? k0 : 0) ? 1u : 0u, bar_empty + 8 * slot);
             }
             if (!ok) break;
             ptx::tc_commit_elect(bar_tfull + 8 * b);

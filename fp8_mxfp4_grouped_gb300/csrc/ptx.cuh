@@ -359,6 +359,40 @@ __device__ __forceinline__ void mma_mxf8f6f4_1x_elect(uint32_t d_tmem, uint64_t 
         : "memory");
 }
 
+// One stage of a single-CTA main loop under a single election: the stage's
+// weight- and token-scale copies to TMEM, its four K = 32 block-scaled MMAs
+// (operands of MMA kk 32 bytes further on: +2 in the descriptors' address
+// field) and the commit that releases the stage.  `accumulate` applies to
+// the first MMA only (the others always accumulate).
+__device__ __forceinline__ void stage_elect(uint32_t d_tmem, uint32_t sfa_tmem, uint64_t sfa_desc,
+                                            uint32_t sfb_tmem, uint64_t sfb_desc, uint64_t a_desc,
+                                            uint64_t b_desc, uint32_t idesc0, uint32_t idesc1,
+                                            uint32_t idesc2, uint32_t idesc3, uint32_t accumulate,
+                                            uint32_t empty_bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %11, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "add.s64 a1, %5, 2;\n\tadd.s64 a2, %5, 4;\n\tadd.s64 a3, %5, 6;\n\t"
+        "add.s64 b1, %6, 2;\n\tadd.s64 b2, %6, 4;\n\tadd.s64 b3, %6, 6;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%1], %2;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%3], %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], %5, %6, %7, [%1], [%3], p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], a1, b1, %8, [%1], [%3], t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], a2, b2, %9, [%1], [%3], t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], a3, b3, %10, [%1], [%3], t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t}" ::"r"(
+            d_tmem),
+        "r"(sfa_tmem), "l"(sfa_desc), "r"(sfb_tmem), "l"(sfb_desc), "l"(a_desc), "l"(b_desc),
+        "r"(idesc0), "r"(idesc1), "r"(idesc2), "r"(idesc3), "r"(accumulate), "r"(empty_bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
