@@ -130,37 +130,44 @@ struct GemmCfg {
 };
 
 // CTA-pair shape (tcgen05 cta_group::2).  T: largest token tile (MMA N,
-// multiple of 32, split in halves between the two CTAs); S: ring stages.
-// Each CTA holds its 128 weight rows and half of the token tile per stage, so
-// a pair computes a 256 x T tile with one MMA instruction stream.
-// Token scales travel in groups of kSfbGroup stages: an activation scale
-// covers a whole 128-K stage, so the four bytes of a TMEM scale word, which
-// the MMA selects by its B scale-factor id, can carry four stages' scales of
-// one token instead of one stage's scale four times.  One copy to TMEM per
-// group then replaces one per stage (the per-stage token-scale copies of
-// CTA pairs measured 6-7 % of the launch at large M on GB300).
-template <int T, int S, int C>
+// multiple of 32, split in halves between the two CTAs); S: ring stages; KB:
+// 128-K blocks per stage.  Each CTA holds its 128 weight rows and half of the
+// token tile per block, so a pair computes a 256 x T tile with one MMA
+// instruction stream.  With KB = 2 the MMA warp waits and commits once per
+// eight MMAs instead of four: on CTA pairs the MMA warp's own per-stage work
+// bounds the tensor pipe.
+// Token scales travel in groups of kSfbGroup 128-K blocks: an activation
+// scale covers a whole block, so the four bytes of a TMEM scale word, which
+// the MMA selects by its B scale-factor id, can carry four blocks' scales of
+// one token instead of one block's scale four times.  One copy to TMEM per
+// group then replaces one per block (the per-block token-scale copies of CTA
+// pairs measured 6-7 % of the launch at large M on GB300).
+template <int T, int S, int C, int KB = 1>
 struct PairCfg {
     static constexpr int kTMax = T;
     static constexpr int kHalf = T / 2;
     static constexpr int kStages = S;
     static constexpr int kCtasPerSm = C;
+    static constexpr int kKB = KB;
     static constexpr int kSfWarps = S;      // one per ring slot (see GemmCfg)
     static constexpr int kSfbWarp = 6 + S;  // token scales, one group at a time
     static constexpr int kThreads = 32 * (7 + S);
-    static constexpr int kSfbGroup = 4;     // stages per token-scale group
+    static constexpr int kSfbGroup = 4;     // 128-K blocks per token-scale group
     static constexpr int kSfbSlots = 3;     // token-scale groups in flight
     static constexpr uint32_t kATileBytes = kHalf * kBK;
+    static constexpr uint32_t kWStageBytes = KB * kWTileBytes;
+    static constexpr uint32_t kAStageBytes = KB * kATileBytes;
+    static constexpr uint32_t kSfaStageBytes = KB * kSfaBytes;
     static constexpr int kSfbAtoms = T > 128 ? 2 : 1;
     static constexpr uint32_t kSfbBytes = 512 * kSfbAtoms;
     static constexpr uint32_t kAccCols = T;
     static constexpr uint32_t kTmemCols = 512 / C;
-    static constexpr uint32_t kSfCol0 = 2 * kAccCols;       // weight scales: 4 columns per ring slot
-    static constexpr uint32_t kSfbCol0 = kSfCol0 + 4 * S;   // token scales: 4 per atom per group slot
+    static constexpr uint32_t kSfCol0 = 2 * kAccCols;            // weight scales: 4 columns per block
+    static constexpr uint32_t kSfbCol0 = kSfCol0 + 4 * KB * S;   // token scales: 4 per atom per group slot
     static constexpr uint32_t kOffW = 0;
-    static constexpr uint32_t kOffA = kOffW + S * kWTileBytes;
-    static constexpr uint32_t kOffSfa = kOffA + S * kATileBytes;
-    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaBytes;   // [group slot] token scales
+    static constexpr uint32_t kOffA = kOffW + S * kWStageBytes;
+    static constexpr uint32_t kOffSfa = kOffA + S * kAStageBytes;
+    static constexpr uint32_t kOffSfb = kOffSfa + S * kSfaStageBytes;   // [group slot] token scales
     // output staging: per epilogue warp two 16-row x 32-column BF16 buffers
     static constexpr uint32_t kOutChunkBytes = 16 * 32 * 2;
     static constexpr uint32_t kOffOut = kOffSfb + kSfbSlots * kSfbBytes;
@@ -178,10 +185,12 @@ struct PairCfg {
     static_assert(smem_bytes(kMaxE) <= kSmemBudget, "shared memory budget");
     static_assert(8 * (2 * S + 5 + 2 * kSfbSlots) <= 256, "barrier area");
     static_assert(C * kThreads * 96 <= 65536, "registers for C resident CTAs");
-    static_assert(kSfbGroup == 4, "four stages per 32-bit scale word");
+    static_assert(kSfbGroup == 4, "four 128-K blocks per 32-bit scale word");
+    static_assert(KB == 1 || KB == 2, "a token-scale group is whole stages");
 };
 
-using CfgPair = PairCfg<224, 5, 1>;     // many rows per expert, N % 256 == 0
+using CfgPair = PairCfg<224, 5, 1>;       // many rows per expert, N % 256 == 0
+using CfgPair2 = PairCfg<224, 3, 1, 2>;   // the same with 256-K stages, K % 256 == 0
 
 using CfgSmall = GemmCfg<64, 4, 2>;    // few rows per expert: HBM-bound weight streaming
 using CfgMid = GemmCfg<112, 3, 2, 1, 2, true>;   // a few hundred rows per expert
@@ -852,7 +861,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     const uint32_t tmem_base = misc[0];
     const Sched sch{s_start, s_rows, s_ntt, s_tile, s_prefix, E, NT, 2 * kBW};
     const int U = s_prefix[E];
-    const int KT = K / kBK;
+    constexpr int KB = Cfg::kKB;
+    const int KT = K / kBK;   // 128-K blocks
+    const int KS = KT / KB;   // stages per unit (K % (128 KB) == 0)
     const WaitCtx wctx{status, misc + 1, timeout_ns};
     // Units u = blockIdx.x / 2 + i * gridDim.x / 2.  The loops read blockIdx
     // and gridDim directly (see the note in grouped_w4a8_kernel on the
@@ -891,7 +902,7 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
             unit_of(u, e, wrow0, row0, nrows, n_mma);
             const int half = n_mma / 2;
             const int wrow = e * N + wrow0 + static_cast<int>(rank) * kBW;
-            for (int ks = 0; ks < KT; ++ks, ++g) {
+            for (int ks = 0; ks < KS; ++ks, ++g) {
                 const uint32_t slot = g % kStages;
                 const uint32_t ph = (g / kStages) & 1u;
                 if (!__all_sync(0xFFFFFFFFu, wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx,
@@ -903,9 +914,13 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 // scale warp issues the activation boxes (more warps issuing
                 // TMA per SM: measured 1-3 % faster at large M)
                 const uint32_t fb = full_tma_leader + 8 * slot;
-                if (leader) ptx::mbar_arrive_expect_tx_elect(fb, 2 * (kWTileTx + half * kBK));
-                ptx::tma_load_2d_pair_elect(sbase + Cfg::kOffW + slot * kWTileBytes, &map_w,
-                                            ks * kBK, wrow, fb, pol_w);
+                if (leader) ptx::mbar_arrive_expect_tx_elect(fb, 2 * KB * (kWTileTx + half * kBK));
+#pragma unroll
+                for (int j = 0; j < KB; ++j) {
+                    ptx::tma_load_2d_pair_elect(
+                        sbase + Cfg::kOffW + slot * Cfg::kWStageBytes + j * kWTileBytes, &map_w,
+                        (ks * KB + j) * kBK, wrow, fb, pol_w);
+                }
             }
         }
         // No copy may land after the CTA exits.  The leader sees its
@@ -941,10 +956,11 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                     ptx::idesc_mxf8f6f4(ptx::kFmtE2M1, ptx::kFmtE4M3, 2 * kBW, n_mma);
                 const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
                 uint32_t gslot = 0, sfb_col = 0;
-                for (int ks = 0; ks < KT; ++ks, ++g) {
+                for (int ks = 0; ks < KS; ++ks, ++g) {
                     const uint32_t slot = g % kStages;
                     const uint32_t ph = (g / kStages) & 1u;
-                    if ((ks & (Cfg::kSfbGroup - 1)) == 0) {
+                    const int kb0 = ks * KB;   // first 128-K block of the stage
+                    if ((kb0 & (Cfg::kSfbGroup - 1)) == 0) {
                         // a new token-scale group: both CTAs' words to TMEM
                         gslot = gr % Cfg::kSfbSlots;
                         if (!__all_sync(0xFFFFFFFFu,
@@ -969,20 +985,34 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + slot * 4;
-                    const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes;
-                    const uint32_t wsm = sbase + Cfg::kOffW + slot * kWTileBytes;
-                    const uint32_t asm_ = sbase + Cfg::kOffA + slot * Cfg::kATileBytes;
-                    const uint32_t b_id = static_cast<uint32_t>(ks) & (Cfg::kSfbGroup - 1);
-                    static_assert(kBK / 32 == 4, "four K = 32 MMAs per stage");
-                    ptx::pair_stage_elect(d_tmem, sf_col, ptx::desc_sf_32x16(sfa),
-                                          ptx::desc_kmajor_sw128(wsm), ptx::desc_kmajor_sw128(asm_),
-                                          ptx::idesc_with_sf_ids(idesc0, 0, b_id),
-                                          ptx::idesc_with_sf_ids(idesc0, 1, b_id),
-                                          ptx::idesc_with_sf_ids(idesc0, 2, b_id),
-                                          ptx::idesc_with_sf_ids(idesc0, 3, b_id), sfb_col,
-                                          ks != 0 ? 1u : 0u, bar_empty + 8 * slot, 0x3);
-                    if (b_id == Cfg::kSfbGroup - 1 || ks == KT - 1) {
+                    static_assert(kBK / 32 == 4, "four K = 32 MMAs per 128-K block");
+#pragma unroll
+                    for (int j = 0; j < KB; ++j) {
+                        const uint32_t blk = slot * KB + j;   // ring block
+                        const uint32_t sf_col = tmem_base + Cfg::kSfCol0 + blk * 4;
+                        const uint64_t sfa = ptx::desc_sf_32x16(sbase + Cfg::kOffSfa + blk * kSfaBytes);
+                        const uint64_t wd = ptx::desc_kmajor_sw128(sbase + Cfg::kOffW + blk * kWTileBytes);
+                        const uint64_t ad =
+                            ptx::desc_kmajor_sw128(sbase + Cfg::kOffA + blk * Cfg::kATileBytes);
+                        const uint32_t b_id = static_cast<uint32_t>(kb0 + j) & (Cfg::kSfbGroup - 1);
+                        const uint32_t acc = (kb0 + j) != 0 ? 1u : 0u;
+                        if (j + 1 < KB) {
+                            ptx::pair_kblock_elect(d_tmem, sf_col, sfa, wd, ad,
+                                                   ptx::idesc_with_sf_ids(idesc0, 0, b_id),
+                                                   ptx::idesc_with_sf_ids(idesc0, 1, b_id),
+                                                   ptx::idesc_with_sf_ids(idesc0, 2, b_id),
+                                                   ptx::idesc_with_sf_ids(idesc0, 3, b_id), sfb_col, acc);
+                        } else {
+                            ptx::pair_stage_elect(d_tmem, sf_col, sfa, wd, ad,
+                                                  ptx::idesc_with_sf_ids(idesc0, 0, b_id),
+                                                  ptx::idesc_with_sf_ids(idesc0, 1, b_id),
+                                                  ptx::idesc_with_sf_ids(idesc0, 2, b_id),
+                                                  ptx::idesc_with_sf_ids(idesc0, 3, b_id), sfb_col, acc,
+                                                  bar_empty + 8 * slot, 0x3);
+                        }
+                    }
+                    const int kb_last = kb0 + KB - 1;
+                    if ((kb_last & (Cfg::kSfbGroup - 1)) == Cfg::kSfbGroup - 1 || ks == KS - 1) {
                         // the group's last MMA: its buffer and TMEM columns free once done
                         ptx::tc_commit_pair_multicast_elect(bar_sfb_empty + 8 * gslot, 0x3);
                         ++gr;
@@ -1137,14 +1167,17 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
             const uint8_t* wsrc =
                 w_scale + static_cast<size_t>(e * N + wrow0 + static_cast<int>(rank) * kBW + lane) *
                               ws_row;
-            for (int ks = 0; ks < KT; ++ks, ++g) {
+            for (int ks = 0; ks < KS; ++ks, ++g) {
                 if (static_cast<int>(g % Cfg::kSfWarps) != sfw) continue;
                 const uint32_t slot = g % kStages;
                 const uint32_t ph = (g / kStages) & 1u;
-                uint32_t wv[4];
+                uint32_t wv[KB][4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    wv[c] = ldg_u32(wsrc + static_cast<size_t>(32 * c) * ws_row + ks * 4);
+                for (int j = 0; j < KB; ++j) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        wv[j][c] = ldg_u32(wsrc + static_cast<size_t>(32 * c) * ws_row + (ks * KB + j) * 4);
+                    }
                 }
                 if (!__all_sync(0xFFFFFFFFu, wait_bounded<true>(bar_empty + 8 * slot, ph ^ 1u, wctx,
                                                                 kRoleScale, slot))) {
@@ -1153,11 +1186,18 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
                 }
                 // this CTA's half of the token tile, counted on the leader's
                 // full barrier (armed by the leader's producer for both CTAs)
-                load_a_rows<true, true>(map_a, sbase + Cfg::kOffA + slot * Cfg::kATileBytes,
-                                        ks * kBK, row0 + static_cast<int>(rank) * (n_mma / 2),
-                                        n_mma / 2, full_tma_leader + 8 * slot, pol_a);
-                const uint32_t sfa = sbase + Cfg::kOffSfa + slot * kSfaBytes + 16 * lane;
-                sts_v4(sfa, wv[0], wv[1], wv[2], wv[3]);
+#pragma unroll
+                for (int j = 0; j < KB; ++j) {
+                    load_a_rows<true, true>(
+                        map_a, sbase + Cfg::kOffA + slot * Cfg::kAStageBytes + j * Cfg::kATileBytes,
+                        (ks * KB + j) * kBK, row0 + static_cast<int>(rank) * (n_mma / 2), n_mma / 2,
+                        full_tma_leader + 8 * slot, pol_a);
+                }
+#pragma unroll
+                for (int j = 0; j < KB; ++j) {
+                    sts_v4(sbase + Cfg::kOffSfa + slot * Cfg::kSfaStageBytes + j * kSfaBytes + 16 * lane,
+                           wv[j][0], wv[j][1], wv[j][2], wv[j][3]);
+                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -1488,7 +1528,10 @@ size_t gemm_smem_bytes(int variant, int32_t E) {
     switch (variant) {
         case 1: return CfgSmall::smem_bytes(E);
         case 2: return CfgMid::smem_bytes(E);
-        case 4: return CfgPair::smem_bytes(E);
+        case 4: {   // the larger of the two CTA-pair shapes (which one runs depends on K)
+            const size_t a = CfgPair::smem_bytes(E), b = CfgPair2::smem_bytes(E);
+            return a > b ? a : b;
+        }
         case 6: return CfgSplit::smem_bytes(E);
         default: return CfgWide2::smem_bytes(E);
     }
@@ -1498,7 +1541,7 @@ long long gemm_launch_ctas(const GemmArgs& a) {
     switch (a.variant) {
         case 1: return grid_plain<CfgSmall>(a);
         case 2: return grid_plain<CfgMid>(a);
-        case 4: return grid_pair<CfgPair>(a);
+        case 4: return a.K % (CfgPair2::kKB * kBK) == 0 ? grid_pair<CfgPair2>(a) : grid_pair<CfgPair>(a);
         case 6: return grid_cluster<CfgSplit>(a);
         default: return grid_plain<CfgWide2>(a);
     }
@@ -1509,7 +1552,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const CUtensorMap& map_w, con
     switch (a.variant) {
         case 1: return launch_cfg<CfgSmall>(a, map_w, map_a, stream);
         case 2: return launch_cfg<CfgMid>(a, map_w, map_a, stream);
-        case 4: return launch_pair<CfgPair>(a, map_w, map_a, map_out, stream);
+        case 4:   // 256-K stages where K allows (half the MMA warp's waits and commits per MMA)
+            return a.K % (CfgPair2::kKB * kBK) == 0
+                       ? launch_pair<CfgPair2>(a, map_w, map_a, map_out, stream)
+                       : launch_pair<CfgPair>(a, map_w, map_a, map_out, stream);
         case 6: return launch_cluster<CfgSplit>(a, map_w, map_a, stream);
         default: return launch_cfg<CfgWide2>(a, map_w, map_a, stream);
     }

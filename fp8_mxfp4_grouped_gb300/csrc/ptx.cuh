@@ -502,6 +502,34 @@ __device__ __forceinline__ void pair_stage_elect(uint32_t d_tmem, uint32_t sfa_t
         : "memory");
 }
 
+// The same without the commit: one 128-K block of a stage that holds
+// several (the commit follows with the stage's last block).
+__device__ __forceinline__ void pair_kblock_elect(uint32_t d_tmem, uint32_t sfa_tmem,
+                                                  uint64_t sfa_desc, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc0, uint32_t idesc1,
+                                                  uint32_t idesc2, uint32_t idesc3,
+                                                  uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "add.s64 a1, %3, 2;\n\tadd.s64 a2, %3, 4;\n\tadd.s64 a3, %3, 6;\n\t"
+        "add.s64 b1, %4, 2;\n\tadd.s64 b2, %4, 4;\n\tadd.s64 b3, %4, 6;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%1], %2;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], %3, %4, %5, [%1], [%9], p;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], a1, b1, %6, [%1], [%9], t;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], a2, b2, %7, [%1], [%9], t;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], a3, b3, %8, [%1], [%9], t;\n\t}" ::"r"(d_tmem),
+        "r"(sfa_tmem), "l"(sfa_desc), "l"(a_desc), "l"(b_desc), "r"(idesc0), "r"(idesc1),
+        "r"(idesc2), "r"(idesc3), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_2d_elect(const CUtensorMap* map, int32_t x, int32_t y) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
