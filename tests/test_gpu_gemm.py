@@ -110,6 +110,10 @@ def test_one_hot_weights_distinct_expert_scales(cuda_lib, variant):
     (2, 384, 1152, [0, 250, 260]),                        # K = 1152: 9 stages
     (2, 128, 128, [0, 5, 40]),                            # K = 128: a single stage
     (1, 256, 384, [0, 77]),                               # K = 384: 3 stages
+    # K % 256 == 0 with 6 and 10 blocks of 128: CTA pairs run 256-K stages whose last
+    # token-scale group (four blocks) is half full
+    (2, 512, 768, [0, 300, 301]),
+    (3, 256, 1280, [0, 60, 290, 291]),
 ])
 def test_ragged_experts_random_codes(cuda_lib, variant, E, N, K, cuts):
     rng = np.random.default_rng(E * 1000 + K)
