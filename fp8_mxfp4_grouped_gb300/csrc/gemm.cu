@@ -1490,18 +1490,20 @@ int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms
         return 1;
     }
     // Above 48 rows per expert: variant 2 (112-row tiles, two CTAs per SM)
-    // or the large-tile variant (4: CTA pairs; 8 when N % 256 != 0).  A
-    // sweep of every configured shape found the large tile faster from 288
-    // rows per expert up and variant 2 faster at 128-256 rows, except where
-    // balanced experts fill the large tiles evenly (12 experts at 170 rows:
-    // 7.5 % faster).  At most 256 rows per expert a wave model decides:
-    // with every expert at the mean, rounds = units / resident CTAs rounded
-    // up, counted in 224-row tiles of 128 weight rows over two CTAs per SM;
-    // a large-tile round costs 1.25 + 0.0026 * tile rows variant-2 rounds,
-    // and the large tile is taken only for a predicted gain of 14 % or more
-    // (skewed routing leaves more partial tiles than the model counts).
-    const int large = N % (2 * kBW) == 0 ? 4 : 8;
-    if (per > 256) return large;
+    // or the large-tile variant (4: CTA pairs; 8 when N % 256 != 0).
+    // CTA pairs: a sweep of both variants on every configured shape and on
+    // gate/up and down at 80-256 rows per expert (both routings) found the
+    // pairs faster from 112 rows per expert up (5-20 %), variant 2 faster or
+    // level at 85 rows and below, and a split at 96 (variant 2 9 % faster with
+    // balanced experts, the pairs 4 % faster on down): above 100 rows, pairs.
+    if (N % (2 * kBW) == 0) return per > 100 ? 4 : 2;
+    // Variant 8 (single-CTA 224-row tiles) above 256 rows; at most 256 rows
+    // per expert a wave model decides: with every expert at the mean, rounds
+    // = units / resident CTAs rounded up, counted in 224-row tiles of 128
+    // weight rows over two CTAs per SM; a large-tile round costs 1.25 +
+    // 0.0026 * tile rows variant-2 rounds, and the large tile is taken only
+    // for a predicted gain of 14 % or more.
+    if (per > 256) return 8;
     if (num_sms <= 0 || N < kBW) return 2;
     const long long g = 2LL * num_sms;
     const long long blocks = static_cast<long long>(E) * (N / kBW);
@@ -1510,7 +1512,7 @@ int gemm_pick_variant(int32_t E, int32_t N, int32_t K, int32_t rows, int num_sms
     const long long rows8 = ((per + t8 - 1) / t8 + 15) / 16 * 16;
     const long long c2 = (blocks * t2 + g - 1) / g * 10000;
     const long long c8 = (blocks * t8 + g - 1) / g * (12500 + 26 * rows8);
-    return 100 * c8 <= 86 * c2 ? large : 2;
+    return 100 * c8 <= 86 * c2 ? 8 : 2;
 }
 
 int gemm_variant_token_tile(int variant) {

@@ -34,10 +34,11 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     With a device (num_sms > 0, split_ctas = the split-K variant's resident
     CTAs) and at most 32 rows per expert, variant 6 is taken when, counting
     one token tile per active expert, it leaves the busiest CTA at least 15 %
-    fewer stages than variant 1.  Above 256 rows per expert the large-tile
-    variant (4 on CTA pairs, or 8 when N % 256 != 0); from 49 to 256 rows
-    variant 2, unless a wave model with every expert at the mean predicts a
-    gain of 14 % or more for the large tile."""
+    fewer stages than variant 1.  From 49 rows per expert: with N % 256 == 0,
+    CTA pairs (variant 4) above 100 rows per expert and variant 2 below;
+    otherwise variant 8 above 256 rows, and from 49 to 256 rows variant 2
+    unless a wave model with every expert at the mean predicts a gain of 14 %
+    or more for variant 8."""
     per = rows // max(E, 1)
     if per <= 48:
         if num_sms > 0 and rows <= 32 * E and K >= 128 and N >= W_TILE and split_ctas >= SPLIT_CLUSTER:
@@ -51,14 +52,15 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
                 if 20 * c6 <= 17 * c1:
                     return 6
         return 1
-    large = 4 if N % (2 * W_TILE) == 0 else 8
+    if N % (2 * W_TILE) == 0:
+        return 4 if per > 100 else 2
     if per > 256:
-        return large
+        return 8
     if num_sms <= 0 or N < W_TILE:
         return 2
     # wave model with every expert at the mean, in 224-row tiles of 128
-    # weight rows over two CTAs per SM; a large-tile round costs
-    # 1.25 + 0.0026 * tile rows variant-2 rounds; the large tile only for a
+    # weight rows over two CTAs per SM; a variant-8 round costs
+    # 1.25 + 0.0026 * tile rows variant-2 rounds; variant 8 only for a
     # predicted gain of 14 % or more
     g = 2 * num_sms
     blocks = E * (N // W_TILE)
@@ -67,7 +69,7 @@ def pick_variant(E: int, N: int, rows: int, K: int = 0, num_sms: int = 0,
     rows8 = -(-(-(-per // t8)) // 16) * 16
     c2 = -(-(blocks * t2) // g) * 10000
     c8 = -(-(blocks * t8) // g) * (12500 + 26 * rows8)
-    return large if 100 * c8 <= 86 * c2 else 2
+    return 8 if 100 * c8 <= 86 * c2 else 2
 
 
 def expert_tiling(rows_e: int, t_max: int = T_MAX, step: int = MMA_N_STEP):

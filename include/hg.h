@@ -213,9 +213,10 @@ hg_status hg_grouped_w4a8_gemm_mmajor(const uint8_t* a_fp8, const uint8_t* a_sca
  * an expert with r rows is cut into ceil(r / T) tiles of equal size rounded
  * up to 16 rows (32 on CTA pairs).  The choice can depend on the current
  * device's SM count and cluster occupancy, which this asks for when a
- * device is present (without one, the split-K variant is never chosen and
- * the 224-row tiles are used exactly above 256 rows per expert).  Launches
- * nothing; 0 for invalid arguments.
+ * device is present (without one, the split-K variant is never chosen, and
+ * the 224-row tiles are used above 100 rows per expert when N % 256 == 0 and
+ * exactly above 256 rows per expert otherwise).  Launches nothing; 0 for
+ * invalid arguments.
  */
 int32_t hg_gemm_token_tile(int32_t E, int32_t N, int32_t K, int32_t rows);
 

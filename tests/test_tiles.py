@@ -71,28 +71,25 @@ def test_forced_variant_token_tiles():
 
 
 @pytest.mark.parametrize("E,N,K,rows,want", [
-    (12, 6144, 3584, 1024, 2),    # 85 rows per expert: one 112-row tile each, same units
-    (12, 6144, 3584, 1408, 4),    # 117: two 112-row tiles or one 224-row tile, 4 rounds vs 2
-    (12, 6144, 3584, 1792, 4),
-    (12, 6144, 3584, 2048, 4),    # 170 rows per expert: model 0.854 (measured 7.5 % faster)
-    (32, 6144, 2048, 4096, 2),    # 128 rows per expert on the down shape: model 0.863 stays
-    (12, 3584, 3072, 1792, 2),    # 336 units of 224 rows fill 1.1 waves: the 2nd round is wasted
-    (12, 3584, 3072, 2560, 2),    # 213 rows: no predicted gain of 14 %
-    (12, 6144, 3584, 2560, 2),
-    (32, 4096, 6144, 4096, 2),    # 128 rows per expert: 7 rounds vs 4 at 1.58x, below the margin
-    (32, 6144, 2048, 6144, 2),    # 192 rows (gate/up M = 768 measured 9 % faster on variant 2)
-    (32, 6144, 2048, 8192, 2),    # 256 rows (down M = 1024 measured 4 % faster on variant 2)
-    (32, 4096, 6144, 9216, 4),    # 288 rows: above 256, the CTA-pair variant
-    (32, 4096, 6144, 16384, 4),
-    (32, 6144, 2048, 131072, 4),
-    (32, 384, 2048, 131072, 8),   # N % 256 != 0: 224-row tiles on single CTAs
+    (32, 4096, 6144, 2048, 2),    # 64 rows per expert: variant 2 (CTA pairs 9 % slower, measured)
+    (32, 4096, 6144, 3072, 2),    # 96 rows: variant 2 (9 % faster with balanced experts)
+    (32, 4096, 6144, 3200, 2),    # 100 rows: still variant 2
+    (32, 4096, 6144, 3264, 4),    # 102 rows: CTA pairs
+    (32, 4096, 6144, 3584, 4),    # 112 rows (gate/up M = 448, measured 5-13 % faster on pairs)
+    (32, 4096, 6144, 4096, 4),    # 128 rows (gate/up M = 512)
+    (32, 6144, 2048, 6144, 4),    # 192 rows (down M = 768, 11 % faster on pairs)
+    (12, 6144, 3584, 2048, 4),    # 170 rows (config 3 W13 M = 256)
+    (12, 3584, 3072, 2048, 4),    # 170 rows (config 3 W2 M = 256)
+    (12, 3584, 3072, 1024, 2),    # 85 rows (config 3 W2 M = 128, level)
+    (32, 4096, 6144, 131072, 4),
+    (32, 384, 2048, 131072, 8),   # N % 256 != 0: 224-row tiles on single CTAs above 256 rows
+    (32, 384, 2048, 4096, 2),     # N % 256 != 0, 128 rows: variant 2
 ])
-def test_wave_model_variant_choice(E, N, K, rows, want):
-    # with a device of 152 SMs the wave model can move shapes of at most
-    # 256 rows per expert to the large tile; without a device it never does
+def test_large_tile_variant_choice(E, N, K, rows, want):
+    # with N % 256 == 0 the choice depends on the mean rows per expert only;
+    # with a device the same (the wave model only guards variant 8)
     assert T.pick_variant(E, N, rows, K, num_sms=152, split_ctas=296) == want
-    large = 4 if N % 256 == 0 else 8
-    assert T.pick_variant(E, N, rows, K) == (2 if rows // E <= 256 else large)
+    assert T.pick_variant(E, N, rows, K) == want
 
 
 def test_tile_inflation_vs_fixed_128():
