@@ -233,8 +233,9 @@ int32_t hg_gemm_ctas(int32_t E, int32_t N, int32_t K, int32_t rows);
  * Force the GEMM pipeline variant for later calls in this process: 0 = choose
  * automatically (default), 1 = 64-row token tiles with two CTAs per SM,
  * 2 = 112-row tiles with two CTAs per SM, 4 = 224-row tiles on CTA pairs
- * (tcgen05 cta_group::2: 256 weight rows per MMA; used only when
- * N % 256 == 0, else variant 8), 6 = 32-row tiles with two CTAs per SM in
+ * (tcgen05 cta_group::2: 256 weight rows per MMA; stages of 256 K when
+ * K % 256 == 0, else 128 K; used only when N % 256 == 0, else variant 8),
+ * 6 = 32-row tiles with two CTAs per SM in
  * clusters of four that split the K loop of each tile over 1, 2 or 4 CTAs
  * (chosen on the device to even out the work when there are few tiles per
  * CTA; the partial sums are added in a fixed order, so results do not vary
