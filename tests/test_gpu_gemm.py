@@ -124,10 +124,13 @@ def test_ragged_experts_random_codes(cuda_lib, variant, E, N, K, cuts):
     assert_rows_close(bf16_bits(out), ref, f"ragged E={E} N={N} K={K}")
 
 
-def test_max_experts_mostly_empty(cuda_lib, variant):
-    # 512 experts (the limit), most of them empty, a few with 1..40 rows
-    rng = np.random.default_rng(12)
-    E, N, K = 512, 128, 512
+@pytest.mark.parametrize("N,K", [(128, 512), (256, 512), (256, 384)])
+def test_max_experts_mostly_empty(cuda_lib, variant, N, K):
+    # 512 experts (the limit), most of them empty, a few with 1..40 rows; with
+    # N = 256 the CTA-pair kernels run with their largest schedule tables
+    # (256-K stages at K = 512, 128-K stages at K = 384)
+    rng = np.random.default_rng(12 + N + K)
+    E = 512
     sizes = np.zeros(E, dtype=np.int64)
     hot = rng.choice(E, 24, replace=False)
     sizes[hot] = rng.integers(1, 41, 24)
@@ -136,7 +139,7 @@ def test_max_experts_mostly_empty(cuda_lib, variant):
     a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
     out = _run_gemm(cuda_lib, a, a_s, w, w_s, cuts)
     ref = G.grouped_w4a8_gemm(a, a_s, w, w_s, cuts, E, N, K)
-    assert_rows_close(bf16_bits(out), ref, "E=512")
+    assert_rows_close(bf16_bits(out), ref, f"E=512 N={N} K={K}")
     assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
 
 
