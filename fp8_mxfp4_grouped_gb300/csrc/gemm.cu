@@ -19,22 +19,29 @@
 //  * warp roles: warp 0 issues the TMA loads (weights through the
 //    16U4_ALIGN16B unpacking TMA type, activations as bytes in boxes of
 //    128/64/32/16 rows; both with the L2 evict-last hint; no multicast);
-//    up to four scale warps (2, 3, 8, 9) stage the block scales into the
-//    tensor core's scale layout (activation scales are per 128-K, replicated
-//    into the four 32-K blocks they cover; the CTA-pair kernel instead packs
-//    four stages' activation scales into one scale word, staged by a warp of
-//    its own, and picks the byte with the MMA's scale-factor id); warp 1 copies scales to TMEM and
-//    issues tcgen05.mma kind::mxf8f6f4 with block scaling, accumulating FP32
-//    in TMEM; warps 4..7 drain the TMEM accumulator to BF16 with stores cut
-//    at the expert's last row (two accumulator buffers, or one where two
-//    224-row pipelines share an SM's TMEM).
+//    one scale warp per ring slot (2, 3, 8, ...) stages the block scales
+//    into the tensor core's scale layout (activation scales are per 128-K,
+//    replicated into the four 32-K blocks they cover; the CTA-pair kernel
+//    instead packs four 128-K blocks' activation scales into one scale word,
+//    staged by a warp of its own, and picks the byte with the MMA's
+//    scale-factor id) and arrives on the stage's TMA barrier, so the MMA warp
+//    waits on one barrier per stage; warp 1 copies scales to TMEM and issues
+//    tcgen05.mma kind::mxf8f6f4 with block scaling (a stage under one
+//    election), accumulating FP32 in TMEM; warps 4..7 drain the TMEM
+//    accumulator to BF16 with stores cut at the expert's last row (two
+//    accumulator buffers, or one where two 224-row pipelines share an SM's
+//    TMEM; CTA pairs write whole 16-row chunks with TMA tensor stores).
 //  * variants (GemmCfg): token tile, ring depth, CTAs per SM, accumulator
 //    buffers; split-K over clusters of four (partials reduce-scattered
-//    through distributed shared memory); two 128-row weight blocks per unit;
-//    and a CTA-pair kernel (tcgen05 cta_group::2, grouped_w4a8_pair_kernel).
-//    The host picks one from the mean rows per expert, with wave models of
-//    the resident CTAs at the split-K and 112/224-row boundaries
-//    (gemm_pick_variant).
+//    through distributed shared memory); and a CTA-pair kernel (tcgen05
+//    cta_group::2, grouped_w4a8_pair_kernel, stages of 256 K where K
+//    allows).  The host picks one from the mean rows per expert
+//    (gemm_pick_variant): measured thresholds, and wave models of the
+//    resident CTAs for the split-K and single-CTA 224-row variants.
+//  * launched with programmatic dependent launch: barrier set-up, TMEM
+//    allocation and tensor-map prefetch run while the routing plan's last
+//    kernel finishes; griddepcontrol.wait comes before the first read of
+//    expert_offsets.
 //  * every barrier wait is bounded (see wait_bounded).
 #include <cuda_bf16.h>
 
@@ -368,6 +375,11 @@ grouped_w4a8_kernel(const __grid_constant__ CUtensorMap map_w,
         ptx::prefetch_tensormap(&map_w);
         for (int i = 0; i < 4; ++i) ptx::prefetch_tensormap(&map_a.box[i]);
     }
+
+    // Nothing above reads global memory: with programmatic dependent launch
+    // it overlaps the kernel before (the routing plan); from here on the
+    // kernel reads what that kernel wrote.
+    ptx::griddep_wait();
 
     // Per-expert token tiling, from the expert's own row count.
     const int NT = N / kBW;
@@ -815,6 +827,9 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
         ptx::prefetch_tensormap(&map_w);
         for (int i = 0; i < 4; ++i) ptx::prefetch_tensormap(&map_a.box[i]);
     }
+
+    // Nothing above reads global memory (see grouped_w4a8_kernel).
+    ptx::griddep_wait();
 
     // Per-expert token tiling (tiles rounded to 32 rows: two halves of 16k).
     const int NT = N / (2 * kBW);
@@ -1383,15 +1398,23 @@ long long grid_pair(const GemmArgs& a) {
 template <class Cfg>
 cudaError_t launch_cfg(const GemmArgs& a, const CUtensorMap& map_w, const AMaps& map_a,
                        cudaStream_t stream) {
-    const cudaError_t attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
-    if (attr != cudaSuccess) return attr;
+    const cudaError_t smem_attr = set_smem_attr(grouped_w4a8_kernel<Cfg>, Cfg::smem_bytes(Cfg::kMaxExperts));
+    if (smem_attr != cudaSuccess) return smem_attr;
     const long long grid = grid_plain<Cfg>(a);
     if (grid < 1) return cudaSuccess;
-    grouped_w4a8_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
-                               stream>>>(map_w, map_a, a.a_scale, a.w_scale, a.offsets,
-                                         a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out, a.status,
-                                         a.timeout_ns);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::smem_bytes(a.E);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_w4a8_kernel<Cfg>, map_w, map_a, a.a_scale, a.w_scale,
+                              a.offsets, a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out, a.status,
+                              a.timeout_ns);
 }
 
 // Split-K variant: clusters of Cfg::kCluster CTAs, launched with the cluster
@@ -1406,13 +1429,15 @@ cudaError_t launch_cluster(const GemmArgs& a, const CUtensorMap& map_w, const AM
     cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::smem_bytes(a.E);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = Cfg::kCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, grouped_w4a8_kernel<Cfg>, map_w, map_a, a.a_scale,
                               a.w_scale, a.offsets, a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out,
                               a.status, a.timeout_ns);
@@ -1423,11 +1448,20 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& map_w, const AMaps
                         const CUtensorMap* map_out, cudaStream_t stream) {
     const long long grid = grid_pair<Cfg>(a);
     if (grid < 2) return cudaSuccess;
-    grouped_w4a8_pair_kernel<Cfg><<<static_cast<int>(grid), Cfg::kThreads, Cfg::smem_bytes(a.E),
-                                    stream>>>(
-        map_w, map_a, map_out ? *map_out : map_w, map_out ? 1 : 0, a.a_scale, a.w_scale,
-        a.offsets, a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out, a.status, a.timeout_ns);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);   // clusters of two: __cluster_dims__
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::smem_bytes(a.E);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_w4a8_pair_kernel<Cfg>, map_w, map_a,
+                              map_out ? *map_out : map_w, map_out ? 1 : 0, a.a_scale, a.w_scale,
+                              a.offsets, a.E, a.N, a.K, a.rows, a.as_rs, a.as_ks, a.out, a.status,
+                              a.timeout_ns);
 }
 
 }  // namespace

@@ -71,6 +71,9 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ ids, int R, int 
                                     int32_t* __restrict__ offsets,
                                     int32_t* __restrict__ sorted_to_src,
                                     int32_t* __restrict__ src_to_sorted) {
+    // the GEMM that follows may start its prologue now (it waits for this
+    // grid to complete before it reads the offsets)
+    ptx::griddep_launch_dependents();
     extern __shared__ int32_t sm_scat[];
     const int nw = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
@@ -209,6 +212,9 @@ __global__ void __launch_bounds__(kClusterThreads)
 plan_cluster_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
                     int32_t* __restrict__ sorted_to_src, int32_t* __restrict__ src_to_sorted,
                     uint32_t* status) {
+    // the GEMM that follows may start its prologue now (it waits for this
+    // grid to complete before it reads the offsets)
+    ptx::griddep_launch_dependents();
     extern __shared__ int32_t sm_cl[];
     constexpr int nw = kClusterWarps;
     const int warp = threadIdx.x >> 5;

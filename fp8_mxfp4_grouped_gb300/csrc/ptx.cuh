@@ -238,6 +238,19 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
     return r;
 }
 
+// Programmatic dependent launch.  launch_dependents: the next kernel of the
+// stream, when launched with programmatic stream serialization, may start
+// once every CTA of this grid has executed it (or exited).  wait: in such a
+// kernel, block until the preceding grid has completed and its memory
+// operations are visible; it returns at once in a kernel launched the
+// ordinary way.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Whole cluster: arrive (release) and wait (acquire) on the cluster barrier.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::

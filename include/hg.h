@@ -189,7 +189,12 @@ hg_status hg_plan_expert_offsets_noalloc(const int32_t* topk_ids, int32_t M, int
  * per CTA from the device's resident CTA count.  Shapes differ only in FP32
  * rounding (the split-K shape sums the partial products of K ranges in K
  * order); for given arguments on a given device the result is the same on
- * every run.
+ * every run.  The kernel is launched with programmatic dependent launch:
+ * its set-up (barriers, TMEM allocation, tensor-map prefetch) may start
+ * while the kernel before it on `stream` is still running, once that kernel
+ * allows it (hg_plan_expert_offsets' last kernel does); it reads and writes
+ * no global memory until that kernel has completed, so stream order holds
+ * for every argument as with a plain launch.
  */
 hg_status hg_grouped_w4a8_gemm(const uint8_t* a_fp8, const uint8_t* a_scale,
                                const uint8_t* w_fp4, const uint8_t* w_scale,
