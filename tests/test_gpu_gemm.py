@@ -505,3 +505,47 @@ def test_tensor_map_cache_same_address_other_shapes(cuda_lib):
                           f"distinct buffer {i}")
     run(*shapes[0], seed=100)
     assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
+
+
+def test_plan_then_gemm_back_to_back(cuda_lib, variant):
+    """Routing plan and GEMM launched back to back on one stream, two routings
+    alternating in the same offsets buffer, no host synchronisation: each GEMM
+    must read the offsets of the plan just before it (the GEMM is launched with
+    programmatic dependent launch, so its set-up runs while that plan is still
+    executing).  Each output equals the one from plan, synchronise, GEMM."""
+    rng = np.random.default_rng(77)
+    E, N, K, M, k = 16, 256, 512, 96, 4
+    R = M * k
+    a, a_s, w, w_s = _rand_codes(rng, R, K, E, N)
+    a_t, as_t, w_t, ws_t = (torch.from_numpy(x).cuda() for x in (a, a_s, w, w_s))
+    routings = []
+    for skew in (0.0, 3.0):
+        p = np.exp(-skew * np.arange(E) / E)
+        p /= p.sum()
+        ids = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(M)])
+        routings.append(torch.from_numpy(ids.astype(np.int32)).cuda())
+    refs = []
+    for ids in routings:
+        off, _, _ = cuda_lib.hg_plan_expert_offsets(ids, E)
+        torch.cuda.synchronize()
+        refs.append(cuda_lib.hg_grouped_w4a8_gemm(a_t, as_t, w_t, ws_t, off))
+        torch.cuda.synchronize()
+    assert not torch.equal(refs[0], refs[1])
+    ids_buf = torch.empty_like(routings[0])
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    s2d = torch.empty(R, dtype=torch.int32, device="cuda")
+    d2s = torch.empty(R, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(cuda_lib.hg_plan_workspace_bytes(M, k, E), 4), dtype=torch.uint8,
+                     device="cuda")
+    outs = [torch.empty((R, N), dtype=torch.bfloat16, device="cuda") for _ in range(12)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i, o in enumerate(outs):
+            ids_buf.copy_(routings[i % 2])
+            cuda_lib.hg_plan_expert_offsets(ids_buf, E, off, s2d, d2s, ws, stream=s)
+            cuda_lib.hg_grouped_w4a8_gemm(a_t, as_t, w_t, ws_t, off, out=o, stream=s)
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o, refs[i % 2]), f"launch {i}"
+    assert cuda_lib.hg_get_device_status()[0] == cuda_lib.HG_OK
