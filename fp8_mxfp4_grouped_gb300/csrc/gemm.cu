@@ -15,7 +15,9 @@
 //    one 144-token tile, not two 128-row tiles.
 //  * persistent CTAs (one or two per SM, sized to one wave) walk a unit list
 //    (expert, weight-row tile, token tile) built on the device from
-//    expert_offsets; no host sync.
+//    expert_offsets; no host sync.  CTA pairs with at most four rounds of
+//    units give the largest experts an extra token tile where the last
+//    round has room for it.
 //  * warp roles: warp 0 issues the TMA loads (weights through the
 //    16U4_ALIGN16B unpacking TMA type, activations as bytes in boxes of
 //    128/64/32/16 rows; both with the L2 evict-last hint; no multicast);
@@ -56,6 +58,8 @@ constexpr int kBK = 128;              // K per pipeline stage = one activation-s
 constexpr int kBW = 128;              // weight rows per tile (MMA M)
 constexpr int kEpiWarps = 4;
 constexpr int kMaxE = 512;            // scheduler tables live in shared memory
+constexpr int kPairFillRounds = 4;    // CTA pairs: fill the last round up to this many rounds
+static_assert(kMaxE <= 32 * 32, "the last-round fill keeps one bit per expert and lane");
 constexpr uint32_t kWTileBytes = kBW * kBK;    // unpacked E2M1: one byte of smem per element
 // The 16U4_ALIGN16B TMA load writes 8 data bytes into each 16-byte chunk and
 // leaves the other 8 untouched; its transaction count is the packed bytes.
@@ -852,6 +856,46 @@ grouped_w4a8_pair_kernel(const __grid_constant__ CUtensorMap map_w,
     }
     __syncthreads();
     if (warp == 0) {
+        // Few rounds: U units dealt to P pairs leave ceil(U/P) * P - U slots
+        // of the last round idle.  With at most kPairFillRounds rounds, the
+        // experts with the largest tiles (64 rows or more, largest first,
+        // then by index) get one token tile more each, NT units per expert,
+        // as many as fit in those slots: the round count stays and the
+        // largest units shrink (config 3 W2 M = 256: 2.2 rounds, 6 % faster;
+        // level to 3 % slower at 8 rounds and more, so not applied there).
+        int tiles = 0;
+        for (int c = 0; c < E; c += 32) {
+            const int e = c + lane;
+            tiles += __reduce_add_sync(0xFFFFFFFFu, e < E ? s_ntt[e] : 0);
+        }
+        const int P = static_cast<int>(gridDim.x >> 1);
+        const long long U0 = static_cast<long long>(tiles) * NT;
+        const long long rounds = (U0 + P - 1) / P;
+        int extra = rounds <= kPairFillRounds ? static_cast<int>((rounds * P - U0) / NT) : 0;
+        const uint32_t below = (1u << lane) - 1u;
+        uint32_t picked = 0;   // bit c / 32: this lane's expert c + lane got its tile
+        for (int v = kTMax; v >= 64 && extra > 0; v -= 32) {
+            for (int c = 0; c < E && extra > 0; c += 32) {
+                const int e = c + lane;
+                bool pick = false;
+                int ntt2 = 0, tile2 = 0;
+                if (e < E && s_ntt[e] > 0 && s_tile[e] == v && !((picked >> (c >> 5)) & 1u)) {
+                    const int r = s_rows[e];
+                    ntt2 = s_ntt[e] + 1;
+                    tile2 = (((r + ntt2 - 1) / ntt2) + 31) & ~31;
+                    pick = tile2 * (ntt2 - 1) < r;   // the last tile keeps a row
+                }
+                const uint32_t m = __ballot_sync(0xFFFFFFFFu, pick);
+                if (pick && __popc(m & below) < extra) {
+                    picked |= 1u << (c >> 5);
+                    s_ntt[e] = ntt2;
+                    s_tile[e] = tile2;
+                    s_prefix[e] = ntt2 * NT;
+                }
+                extra -= min(extra, __popc(m));
+            }
+        }
+        __syncwarp();
         int carry = 0;
         for (int c = 0; c < E; c += 32) {
             const int e = c + lane;

@@ -93,6 +93,35 @@ def token_tiles(rows_e: int, t_max: int = T_MAX, step: int = MMA_N_STEP):
     return out
 
 
+PAIR_FILL_ROUNDS = 4     # CTA pairs: last-round fill up to this many rounds
+
+
+def pair_tiling(rows_per_expert, N: int, pairs: int, t_max: int = T_MAX):
+    """Per-expert (n_t, tile) of the CTA-pair kernel (variant 4), with its
+    last-round fill: U = sum(n_t) * N/256 units dealt to `pairs` pairs leave
+    ceil(U / pairs) * pairs - U slots of the last round idle; with at most
+    PAIR_FILL_ROUNDS rounds, floor(idle / (N/256)) experts get one token tile
+    more each, taken by tile (64 rows or more, largest first), then by expert
+    index, and only where the extra tile leaves the last one a row."""
+    step = VARIANT_STEP[4]
+    NT = N // (2 * W_TILE)
+    til = [list(expert_tiling(int(r), t_max, step)) for r in rows_per_expert]
+    U0 = sum(n for n, _ in til) * NT
+    rounds = -(-U0 // pairs) if pairs > 0 else 0
+    extra = (rounds * pairs - U0) // NT if 0 < rounds <= PAIR_FILL_ROUNDS and NT > 0 else 0
+    cands = []
+    for e, (n, t) in enumerate(til):
+        if n == 0 or t < 64:
+            continue
+        n2 = n + 1
+        t2 = -(-(-(-int(rows_per_expert[e]) // n2)) // step) * step
+        if t2 * (n2 - 1) < int(rows_per_expert[e]):
+            cands.append((-t, e, n2, t2))
+    for _, e, n2, t2 in sorted(cands)[:max(extra, 0)]:
+        til[e] = [n2, t2]
+    return [tuple(x) for x in til]
+
+
 def units(offsets, N: int, t_max: int = T_MAX):
     """Work units of one launch: (expert, n0, first sorted row, valid rows, mma_n)."""
     E = len(offsets) - 1

@@ -135,3 +135,50 @@ def test_split_choice(U, KT, G, want):
     costs = {s: busiest(s) for s in (1, 2, 4) if KT % s == 0}
     assert costs[want] == min(costs.values())
     assert all(costs[s] > costs[want] for s in costs if s < want)
+
+
+def _pair_units(tiling, N):
+    return sum(n for n, _ in tiling) * (N // 256)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_pair_fill_keeps_rounds_and_covers_rows(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 40))
+    N = 256 * int(rng.integers(1, 30))
+    pairs = int(rng.integers(1, 80))
+    rows = rng.integers(0, 900, E) * (rng.random(E) < 0.8)
+    base = [T.expert_tiling(int(r), 224, 32) for r in rows]
+    filled = T.pair_tiling(rows, N, pairs)
+    U0, U1 = _pair_units(base, N), _pair_units(filled, N)
+    r0 = -(-U0 // pairs)
+    assert -(-U1 // pairs) == r0                     # the round count stays
+    if r0 > T.PAIR_FILL_ROUNDS:
+        assert filled == base
+    for r, (n0, t0), (n, t) in zip(rows, base, filled):
+        assert n - n0 in (0, 1)                      # at most one extra tile per expert
+        if r == 0:
+            assert (n, t) == (0, 0)
+            continue
+        assert t % 32 == 0 and t <= 224 and n * t >= r and (n - 1) * t < r
+        if n > n0:
+            assert t0 >= 64
+    extra = sum(n - n0 for (n0, _), (n, _) in zip(base, filled))
+    assert extra * (N // 256) <= r0 * pairs - U0 if r0 <= T.PAIR_FILL_ROUNDS else extra == 0
+
+
+def test_pair_fill_worked_example():
+    # config 3 W2 shape: 12 experts of 170 rows, N = 3584 (14 weight-tile pairs),
+    # 76 pairs: 168 units, 3 rounds, 60 idle slots -> 4 experts get a second tile
+    got = T.pair_tiling([170] * 12, 3584, 76)
+    assert got == [(2, 96)] * 4 + [(1, 192)] * 8
+    # largest tiles first, then index; tiles under 64 rows never split
+    got = T.pair_tiling([40, 300, 230, 100, 229], 256, 12)
+    # base: (1,64) (2,160) (2,128) (1,128) (2,128): 8 units, 1 round, 4 idle -> the
+    # 160-row expert, then the three 128-row ones; the 64-row expert stays whole
+    assert got == [(1, 64), (3, 128), (3, 96), (2, 64), (3, 96)]
+    got = T.pair_tiling([40, 300, 230, 100, 229], 256, 10)
+    # 8 units, 1 round of 10: 2 idle -> the 160-row expert, then expert 2 (128, lowest index)
+    assert got == [(1, 64), (3, 128), (3, 96), (1, 128), (2, 128)]
+    # eight or more rounds: unchanged
+    assert T.pair_tiling([170] * 12, 3584, 20) == [(1, 192)] * 12
