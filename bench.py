@@ -359,7 +359,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_min": min(sm)}
 
 
 # ---------------------------------------------------------------- our arm --
@@ -560,9 +560,14 @@ def run_ours(args, rank, world):
     moe_io = None if args.no_moe_io else time_moe_io(cases[-1], flush, stream, peaks, hg)
 
     others = None
+    clk_others = None
     if default_workload(args) and not args.no_other_workloads:
+        # clocks sampled while the other workloads run, for reading their numbers
+        sampler = ClockSampler(torch.cuda.current_device())
+        sampler.start()
         others = time_other_workloads(flush, stream, peaks, fp8_peak, hg,
                                       reps=max(5, min(args.steps, 20)))
+        clk_others = sampler.stop()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -586,6 +591,7 @@ def run_ours(args, rank, world):
         "gpu_launches": sum(hg.hg_plan_launches(cs["M"], cs["c"].top_k, cs["c"].E) + 1
                             for cs in cases) * args.steps,
         "clocks": clk,
+        "clocks_other_workloads": clk_others,
         "wall_s_timed": round(t_wall, 3),
     }
     return line
