@@ -308,58 +308,121 @@ def barrier(world):
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling in the background during timing."""
+    """SM clock and clock-event reasons of the benchmarked GPU, sampled in the
+    background while timing (read-only queries).  The GPU is found by its PCI
+    bus id, so the samples follow the CUDA device even when device indices are
+    remapped.  NVML through ctypes polls every 50 ms; without NVML,
+    nvidia-smi does every 200 ms."""
 
+    REASONS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+               ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index=0):
+    def __init__(self, index=0, period_s=0.05):
+        self.period_s = period_s
+        self.bus = None
+        try:
+            pr = torch.cuda.get_device_properties(index)
+            self.bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+        except Exception:
+            pass
         self.index = index
+        self.samples = []     # (sm_mhz, reason names)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+        self.thread = None
         self.proc = None
-        self.lines = []
+
+    # -- NVML (libnvidia-ml, read-only calls)
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if self.bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(
+                self.bus.encode(), ctypes.byref(h)) != 0:
+            return None
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # 1 = SM clock
+            self.max_mhz = float(mx.value)
+        return lib, h, get_reasons
+
+    def _nvml_loop(self, lib, h, get_reasons):
+        import ctypes
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    get_reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value),
+                                     [n for n, bit in self.REASONS if rs.value & bit]))
+            self._stop.wait(self.period_s)
+        lib.nvmlShutdown()
+
+    # -- nvidia-smi fallback
+    def _smi_loop(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm, mx = float(f[0]), float(f[1])
+            except ValueError:
+                continue
+            self.max_mhz = mx
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            self.samples.append((sm, [n for n, v in zip(names, f[4:8])
+                                      if v.lower().startswith("active")]))
 
     def start(self):
         try:
+            opened = self._nvml_open()
+        except (OSError, AttributeError):
+            opened = None
+        if opened is not None:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._nvml_loop, args=opened, daemon=True)
+            self.thread.start()
+            return
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                ["nvidia-smi", "-i", self.bus or str(self.index), f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._smi_loop, daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
-        if self.proc is None:
+        if self.source is None:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 8:
-                continue
+        self._stop.set()
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(f[0]))
-                mx = float(f[1])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        return self.summary(self.samples, self.max_mhz, self.source, self.bus)
+
+    @staticmethod
+    def summary(samples, max_mhz, source, bus):
+        if not samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm), "sm_mhz_min": min(sm)}
+        sm = [x for x, _ in samples]
+        reasons = sorted({n for _, names in samples for n in names})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max_mhz, "reasons": reasons,
+                "samples": len(sm), "sm_mhz_min": min(sm), "source": source, "gpu_pci": bus}
 
 
 # ---------------------------------------------------------------- our arm --
