@@ -557,7 +557,7 @@ def run_ours(args, rank, world):
     # and a third's download.
     e2e = None
     if not args.no_e2e:
-        e_streams = [torch.cuda.Stream() for _ in range(3)]
+        e_streams = [torch.cuda.Stream() for _ in range(max(1, args.e2e_streams))]
         for cs in cases:
             c = cs["c"]
             cs["host_ws"] = torch.empty(
@@ -618,7 +618,7 @@ def run_ours(args, rank, world):
                    host_link_gbs=link,
                    copy_floor_ms=round((bi + bo) / (link["both"] * 1e9) * 1e3, 3),
                    note="hg_grouped_w4a8_gemm_host per batch (pinned host buffers, the library "
-                        "copies); batches on three streams in turn")
+                        f"copies); batches on {len(e_streams)} streams in turn")
 
     moe_io = None if args.no_moe_io else time_moe_io(cases[-1], flush, stream, peaks, hg)
 
@@ -817,6 +817,8 @@ def main(argv=None):
     ap.add_argument("--proj", default=None)
     ap.add_argument("--routing", default=None)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="streams the end-to-end leg deals its batches to, in turn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe-io", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true")
