@@ -281,11 +281,17 @@ def test_split_k_config3_small_m(cuda_lib, M, proj):
 
 # ------------------------------------------------ full-size sampled parity --
 
-def _sample_rows(off, rng, t_max, per_expert=3, max_experts=6):
-    """Expert boundaries, token-tile boundaries and random rows of a few experts."""
-    from fp8_mxfp4_grouped_gb300.tiles import token_tiles
+def _sample_rows(off, rng, t_max, per_expert=3, max_experts=6, pair_n=0):
+    """Expert boundaries, token-tile boundaries and random rows of a few experts.
+    With pair_n = N (CTA pairs), also the tile boundaries after the pair kernel's
+    last-round fill on this device's pairs."""
+    from fp8_mxfp4_grouped_gb300.tiles import pair_tiling, token_tiles
     off = np.asarray(off)
     sizes = np.diff(off)
+    filled = None
+    if pair_n:
+        pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+        filled = pair_tiling(sizes, pair_n, pairs)
     nz = np.nonzero(sizes)[0]
     pick = set([int(nz[np.argmax(sizes[nz])]), int(nz[np.argmin(sizes[nz])])])
     pick |= set(int(x) for x in rng.choice(nz, size=min(len(nz), max_experts - 2), replace=False))
@@ -297,6 +303,10 @@ def _sample_rows(off, rng, t_max, per_expert=3, max_experts=6):
         for step in ((16, 32) if t_max == 224 else (16,)):
             for r0, valid, _ in token_tiles(hi - lo, t_max, step):
                 rows |= {lo + r0, lo + r0 + valid - 1}
+        if filled is not None and filled[e][0] > 0:
+            n_t, tile = filled[e]
+            for tt in range(n_t):
+                rows |= {lo + tt * tile, min(hi, lo + (tt + 1) * tile) - 1}
         rows |= set(int(x) for x in rng.integers(lo, hi, per_expert))
     return np.array(sorted(rows), dtype=np.int64)
 
@@ -321,7 +331,9 @@ def test_full_size_sampled_rows(cuda_lib, cid, M, proj, routing):
     off, *_ = plan_expert_offsets(c.topk_ids, c.E)
     assert np.array_equal(off_t.cpu().numpy(), off)
     rng = np.random.default_rng(cid * 100000 + M)
-    rows = _sample_rows(off, rng, cuda_lib.hg_gemm_token_tile(c.E, c.N, c.K, c.R))
+    t_max = cuda_lib.hg_gemm_token_tile(c.E, c.N, c.K, c.R)
+    pair = t_max == 224 and c.N % 256 == 0 and c.R // c.E > 100
+    rows = _sample_rows(off, rng, t_max, pair_n=c.N if pair else 0)
     rr = torch.from_numpy(rows).cuda()
     a = c.a_fp8[rr].cpu().numpy()
     a_s = c.a_scale[rr].cpu().numpy()
